@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark: one step = route metadata + dispatch (gather, fused quantisation) + weighted
+combine over one batch of a seeded synthetic workload, on one GB300 per rank.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|qwen3|nvfp4|tiny]
+                    [--impl ours|reference] [--graph]
+
+Prints ONE JSON line (rank 0). ``value`` is whole-job dispatch+combine throughput in tokens/s
+(tokens of all ranks / max-over-ranks mean step time), inputs resident in HBM, L2 flushed
+(256 MiB write) before every step. ``e2e`` repeats the measurement through the public Python
+API with pinned host inputs copied in and the combined output copied out inside the timed
+region. ``roofline`` reports the dominant kernel's algorithmic bytes / CUDA-event duration
+against the measured HBM copy bandwidth. ``cpu_baseline`` times the CPU oracle on a bounded
+sample of the same workload. ``--impl reference`` times that oracle as the reference arm.
+Multi-GPU: one process per GPU (torchrun), each rank runs its own seeded batch (weak
+scaling, no data-path collective; a max-reduce of the step time only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (fraction of ~8 TB/s), 1 GB300"
+FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = {
+    "route_meta": "combine_moe_route_meta_gb300/csrc/route_meta.cu",
+    "dispatch": "combine_moe_route_meta_gb300/csrc/dispatch.cu",
+    "combine": "combine_moe_route_meta_gb300/csrc/combine.cu",
+}
+
+
+# ---------------------------------------------------------------------------
+# byte model (algorithmic bytes each kernel must move; padding/capacity never counted)
+# ---------------------------------------------------------------------------
+
+def row_bytes(quant: str, H: int) -> int:
+    if quant == "none":
+        return 2 * H
+    if quant == "fp8g128":
+        return H + 4 * (H // 128)
+    return H // 2 + H // 16
+
+
+def algorithmic_bytes(w, n_valid: int, n_rows: int) -> dict:
+    """n_valid: valid pairs; n_rows: rows actually written by dispatch / read by combine."""
+    T, H, K, E = w.T, w.H, w.K, w.E
+    masked = w.mode == "masked"
+    meta = 4 * T * K + 4 * T * K + 4 * n_valid + 8 * (E + 1) + 4 * E + 4 * w.P
+    disp = 2 * T * H + 4 * T * K + (4 * T * K + 8 * E if masked else 0) + n_rows * row_bytes(w.quant, H)
+    comb = n_rows * 2 * H + 8 * T * K + (4 * T * K + 8 * E if masked else 0) + 2 * T * H
+    return {"route_meta": meta, "dispatch": disp, "combine": comb}
+
+
+def measured_hbm_gbs():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(kernel: str) -> str:
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kernel]), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    fields = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.lstrip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("source_sha256") != source_digest(kernel):
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_step(w, T_s: int, expert_rows):
+    """One oracle pass (route meta + dispatch + combine) over the first T_s tokens."""
+    import oracle
+    ids = np.ascontiguousarray(w.topk_ids[:T_s])
+    x = np.ascontiguousarray(w.x[:T_s])
+    wt = np.ascontiguousarray(w.topk_weights[:T_s])
+    meta = oracle.route_meta(ids, w.E, P=w.P, M=w.M)
+    rows = None if w.mode == "masked" else T_s * w.K
+    oracle.dispatch(w.mode, w.quant, x, ids, meta, w.E, M=w.M, global_scale=w.global_scale or 0.0, rows=rows)
+    if w.mode == "normal":
+        eo = expert_rows[: max(meta.num_valid, 1)]
+        oracle.combine("normal", eo, ids, wt, meta, w.E)
+    else:
+        # masked combine reads only rows e*M + rank < e*M + masked_m[e]; give it a layout
+        # whose experts hold just the slots this sample fills
+        M_s = int(meta.masked_m.max()) if meta.num_valid else 1
+        meta_s = oracle.route_meta(ids, w.E, P=w.P, M=M_s)
+        eo = expert_rows[: w.E * M_s]
+        oracle.combine("masked", eo, ids, wt, meta_s, w.E, M=M_s)
+
+
+def time_oracle(w, budget_s: float, max_tokens: int):
+    """Pick a token sample that takes ~budget_s per step and time one step of it."""
+    from workloads import random_bf16
+    rng = np.random.default_rng(99)
+    T_probe = min(w.T, 16)
+    er = random_bf16(rng, (max(w.E * max(T_probe, 1), T_probe * w.K, 1), w.H))
+    t0 = time.perf_counter()
+    oracle_step(w, T_probe, er)
+    per_tok = (time.perf_counter() - t0) / T_probe
+    T_s = int(max(1, min(w.T, max_tokens, budget_s / max(per_tok, 1e-9))))
+    er = random_bf16(rng, (max(w.E * T_s, T_s * w.K, 1), w.H))
+    return T_s, er
+
+
+def cpu_baseline(w, budget_s: float = 12.0) -> dict:
+    T_s, er = time_oracle(w, budget_s / 3, w.T)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        oracle_step(w, T_s, er)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end or len(times) >= 50:
+            break
+    med = statistics.median(times)
+    return {"value": T_s / med, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {T_s} of {w.T} tokens of the {w.name} workload, route+dispatch+combine, "
+                      f"median of {len(times)} passes, single-threaded C oracle"}
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return None
+    total_steps = args.steps + args.warmup
+    budget = max(0.05, min(5.0, 90.0 / max(total_steps, 1)))
+    T_s, er = time_oracle(w, budget, w.T)
+    for _ in range(args.warmup):
+        oracle_step(w, T_s, er)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, T_s, er)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = T_s / (ms / 1e3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 combine / f32 quant", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {T_s} of {w.T} tokens per step, route+dispatch+combine, "
+                                   f"single-threaded C oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(x: float, dist, device="cpu") -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own batch of the workload (weak scaling)."""
+    return rank
+
+
+def config_of(w) -> dict:
+    return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "P": w.P, "M": w.M,
+            "mode": w.mode, "quant": w.quant, "seed": w.seed, "recipe": w.recipe,
+            "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write)"}
+
+
+def run_gpu(args, w, rank, world, dist):
+    import torch
+    import combine_moe_route_meta_gb300 as moe
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x_h = torch.from_numpy(w.x.view(np.int16)).view(torch.bfloat16)
+    ids_h = torch.from_numpy(w.topk_ids)
+    wt_h = torch.from_numpy(w.topk_weights)
+    x, ids, wt = x_h.to(dev), ids_h.to(dev), wt_h.to(dev)
+    d = moe.MoEDispatcher(w.T, w.H, w.K, w.E, mode=w.mode, quant=w.quant, num_partitions=w.P,
+                          max_tokens_per_expert=w.M, device=dev)
+    g = w.global_scale or 0.0
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+    eo_rows = w.T * w.K if w.mode == "normal" else w.E * w.M
+    expert_out = torch.randn((eo_rows, w.H), dtype=torch.bfloat16, device=dev, generator=gen)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    route_launches = 1 if moe.moe_route_meta_workspace_size(w.T, w.K, w.E) == 0 else 2
+
+    def step():
+        d.route(ids)
+        d.dispatch(x, ids, g)
+        d.combine(expert_out, ids, wt)
+
+    # metadata facts for the byte model
+    step()
+    torch.cuda.synchronize()
+    d.check()
+    seg = d.seg_indptr.cpu().numpy()
+    n_valid = int(seg[-1])
+    n_rows = int(d.masked_m.sum().item()) if w.mode == "masked" else n_valid
+    algo = algorithmic_bytes(w, n_valid, n_rows)
+
+    graph = None
+    if args.graph:
+        s = torch.cuda.Stream()
+        s.wait_stream(stream)
+        with torch.cuda.stream(s):
+            step()
+        stream.wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        graph.replay() if graph else step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        e = ev[i]
+        if graph:
+            e[0].record(stream)
+            graph.replay()
+            e[3].record(stream)
+        else:
+            e[0].record(stream)
+            d.route(ids)
+            e[1].record(stream)
+            d.dispatch(x, ids, g)
+            e[2].record(stream)
+            d.combine(expert_out, ids, wt)
+            e[3].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    d.check()
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
+    value = job_throughput(w.T, world, ms)
+
+    kernels = {}
+    if not graph:
+        for name, (a, b) in {"route_meta": (0, 1), "dispatch": (1, 2), "combine": (2, 3)}.items():
+            us = 1e3 * statistics.mean(e[a].elapsed_time(e[b]) for e in ev)
+            kernels[name] = {"us": us, "bytes": algo[name], "gbs": algo[name] / (us * 1e-6) / 1e9}
+    peak, peak_kind = measured_hbm_gbs()
+    roofline = None
+    if kernels:
+        dom = max(kernels, key=lambda k: kernels[k]["us"])
+        ach = kernels[dom]["gbs"]
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
+                    "frac": ach / peak, "peak_source": f"{peak_kind} (hbm_gbs copy bandwidth)",
+                    "algorithmic_bytes_per_launch": algo[dom],
+                    "traffic": profiled_traffic(dom, w.name)}
+    step_bytes = sum(algo.values())
+
+    # ---- end to end through the public API: pinned host in, host out ----
+    e2e = None
+    if not args.no_e2e:
+        xp, idp, wtp = x_h.pin_memory(), ids_h.pin_memory(), wt_h.pin_memory()
+        outp = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+        x2, ids2, wt2 = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(wt)
+
+        def e2e_step():
+            x2.copy_(xp, non_blocking=True)
+            ids2.copy_(idp, non_blocking=True)
+            wt2.copy_(wtp, non_blocking=True)
+            d.route(ids2)
+            d.dispatch(x2, ids2, g)
+            y = d.combine(expert_out, ids2, wt2)
+            outp.copy_(y, non_blocking=True)
+
+        for _ in range(max(args.warmup, 1)):
+            flush.fill_(1)
+            e2e_step()
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            ev2[i][0].record(stream)
+            e2e_step()
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        d.check()
+        ms2 = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev2), dist, dev)
+        h2d = x_h.numel() * 2 + ids_h.numel() * 4 + wt_h.numel() * 4
+        e2e = {"value": job_throughput(w.T, world, ms2), "unit": "tokens/s", "ms_per_step": ms2,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": w.T * w.H * 2}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy PCG64 inputs, random expert outputs)",
+        "config": dict(config_of(w), graph=bool(graph), n_valid_pairs=n_valid, rows_moved=n_rows),
+        "achieved_gbs_step": step_bytes / (ms * 1e-3) / 1e9 / max(world, 1) * world,
+        "step_algorithmic_bytes": step_bytes,
+        "kernels": kernels,
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (route_launches + 2),
+        "clocks": clocks,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "qwen3", "nvfp4"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--graph", action="store_true", help="replay the three launches as one CUDA graph")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from workloads import make_workload
+
+    if args.impl == "reference":
+        w = make_workload(args.workload, seed=0)
+        line = run_reference(args, w, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+
+    from combine_moe_route_meta_gb300 import build as _build
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    if dist:
+        dist.barrier()
+
+    w = make_workload(args.workload, seed=rank_seed(rank))
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+    line = run_gpu(args, w, rank, world, dist)
+    line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,335 @@
+"""GB300 (sm_103a) MoE token dispatch / combine.
+
+Python binding of the C ABI in ``include/moe_dispatch.h``. The functions named like
+the C entry points (``moe_route_meta``, ``moe_dispatch``, ``moe_combine``, ...) only
+marshal arguments: every step of the path runs in the CUDA kernels of
+``libmoe_dispatch.so``. PyTorch supplies device memory and streams.
+
+The higher-level helpers (:func:`route_meta`, :func:`dispatch`, :func:`combine`,
+:class:`MoEDispatcher`) allocate outputs with torch and return named tuples shaped
+like the dispatcher pages' outputs (``DeepEPNormalDispatchOutput`` /
+``DeepEPLLDispatchOutput`` on the "sglang token_dispatcher/deepep.py" page).
+
+There is no CPU fallback: the first call raises when the library has not been built
+(``python -m combine_moe_route_meta_gb300.build``), and every call requires CUDA tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_dispatch.so")
+
+# ---------------------------------------------------------------------------
+# C ABI constants (mirrors include/moe_dispatch.h)
+# ---------------------------------------------------------------------------
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CAPACITY = 3
+MOE_ERR_BAD_EXPERT_ID = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_CUDA = 6
+
+MOE_MODE_NORMAL = 0
+MOE_MODE_MASKED = 1
+MODES = {"normal": MOE_MODE_NORMAL, "masked": MOE_MODE_MASKED}
+
+MOE_QUANT_NONE = 0
+MOE_QUANT_FP8_G128 = 1
+MOE_QUANT_NVFP4_B16 = 2
+QUANTS = {"none": MOE_QUANT_NONE, "fp8g128": MOE_QUANT_FP8_G128, "nvfp4b16": MOE_QUANT_NVFP4_B16}
+
+MOE_MAX_EXPERTS = 1024
+MOE_MAX_TOPK = 16
+
+_P = ctypes.c_void_p
+_i32, _i64, _int, _f32, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+_SIGNATURES = {
+    "moe_abi_version": (_int, []),
+    "moe_status_string": (ctypes.c_char_p, [_int]),
+    "moe_route_meta_workspace_size": (_sz, [_i64, _int, _int]),
+    "moe_route_meta": (_int, [_P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P, _sz, _P, _P]),
+    "moe_dispatch": (_int, [_int, _int, _P, _i64, _int, _P, _int, _int, _int, _P, _P, _f32, _P, _P, _P, _P]),
+    "moe_combine": (_int, [_int, _P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_convert_probe": (_int, [_P, _i64, _P, _P, _P, _P]),
+}
+_lib_handle = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libmoe_dispatch.so (once). Raises when it has not been built: no CPU fallback."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(python -m combine_moe_route_meta_gb300.build); there is no CPU fallback")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib_handle = lib
+    return _lib_handle
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = int(status)
+        super().__init__(f"{where}: {moe_status_string(status)}" if where else moe_status_string(status))
+
+
+def moe_status_string(status: int) -> str:
+    return load_library().moe_status_string(int(status)).decode()
+
+
+def moe_abi_version() -> int:
+    return int(load_library().moe_abi_version())
+
+
+def moe_route_meta_workspace_size(num_tokens: int, topk: int, num_experts: int) -> int:
+    return int(load_library().moe_route_meta_workspace_size(int(num_tokens), int(topk), int(num_experts)))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensor expected (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoEError(status, where)
+
+
+# ---------------------------------------------------------------------------
+# thin wrappers with the C names
+# ---------------------------------------------------------------------------
+
+def moe_route_meta(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torch.Tensor,
+                   src2dst: torch.Tensor, reorder_topk_ids: torch.Tensor, masked_m: torch.Tensor,
+                   dev_status: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                   num_partitions: int = 1, max_tokens_per_expert: int = 0,
+                   partition_counts: Optional[torch.Tensor] = None, stream=None) -> int:
+    """Launch moe_route_meta; returns expected_m (computed on the host)."""
+    T, K = topk_ids.shape
+    em = ctypes.c_int32(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load_library().moe_route_meta(_ptr(topk_ids), T, K, num_experts, num_partitions, max_tokens_per_expert,
+                             _ptr(seg_indptr), _ptr(src2dst), _ptr(reorder_topk_ids), _ptr(masked_m),
+                             _ptr(partition_counts), ctypes.byref(em), _ptr(workspace), ws_bytes,
+                             _ptr(dev_status), _stream(stream))
+    _check(st, "moe_route_meta")
+    return int(em.value)
+
+
+def moe_dispatch(mode: str, quant: str, hidden_states: torch.Tensor, topk_ids: torch.Tensor,
+                 num_experts: int, src2dst: torch.Tensor, seg_indptr: torch.Tensor,
+                 out_q: torch.Tensor, out_scales: Optional[torch.Tensor], dev_status: torch.Tensor,
+                 max_tokens_per_expert: int = 0, input_global_scale: float = 0.0, stream=None) -> None:
+    T, H = hidden_states.shape
+    K = topk_ids.shape[1]
+    st = load_library().moe_dispatch(MODES[mode], QUANTS[quant], _ptr(hidden_states), T, H, _ptr(topk_ids), K,
+                           num_experts, max_tokens_per_expert, _ptr(src2dst), _ptr(seg_indptr),
+                           float(input_global_scale), _ptr(out_q), _ptr(out_scales), _ptr(dev_status),
+                           _stream(stream))
+    _check(st, "moe_dispatch")
+
+
+def moe_combine(mode: str, expert_out: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                num_experts: int, src2dst: torch.Tensor, seg_indptr: torch.Tensor, out: torch.Tensor,
+                dev_status: torch.Tensor, max_tokens_per_expert: int = 0, stream=None) -> None:
+    T, K = topk_ids.shape
+    H = out.shape[1]
+    st = load_library().moe_combine(MODES[mode], _ptr(expert_out), T, H, K, num_experts, max_tokens_per_expert,
+                          _ptr(topk_ids), _ptr(src2dst), _ptr(seg_indptr), _ptr(topk_weights), _ptr(out),
+                          _ptr(dev_status), _stream(stream))
+    _check(st, "moe_combine")
+
+
+def moe_convert_probe(x: torch.Tensor, e4m3: Optional[torch.Tensor] = None, e2m1: Optional[torch.Tensor] = None,
+                      e4m3_value: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Diagnostics: the quantisers' e4m3 / e2m1 conversions applied to fp32 values ``x``."""
+    st = load_library().moe_convert_probe(_ptr(x), x.numel(), _ptr(e4m3), _ptr(e2m1), _ptr(e4m3_value), _stream(stream))
+    _check(st, "moe_convert_probe")
+
+
+# ---------------------------------------------------------------------------
+# convenience layer: allocates outputs, returns the pages' tuple shapes
+# ---------------------------------------------------------------------------
+
+class RouteMeta(NamedTuple):
+    seg_indptr: torch.Tensor        # int64 [E+1]
+    src2dst: torch.Tensor           # int32 [T*K]
+    reorder_topk_ids: torch.Tensor  # int32 [T*K]; first seg_indptr[E] entries valid
+    masked_m: torch.Tensor          # int32 [E]
+    partition_counts: torch.Tensor  # int32 [P]
+    expected_m: int
+
+
+class NormalDispatchOutput(NamedTuple):
+    """Expert-contiguous dispatch (DeepEPNormalDispatchOutput with the permute metadata)."""
+    hidden_states: torch.Tensor            # [T*K (capacity), H] bf16 / [.., H] uint8 / [.., H/2] uint8
+    hidden_states_scale: Optional[torch.Tensor]
+    topk_ids: torch.Tensor
+    topk_weights: torch.Tensor
+    seg_indptr: torch.Tensor
+    reorder_topk_ids: torch.Tensor
+    src2dst: torch.Tensor
+
+
+class LLDispatchOutput(NamedTuple):
+    """Masked-layout dispatch (DeepEPLLDispatchOutput)."""
+    hidden_states: torch.Tensor            # [E, M, H] bf16 / [E, M, H] uint8 / [E, M, H/2] uint8
+    hidden_states_scale: Optional[torch.Tensor]
+    topk_ids: torch.Tensor
+    topk_weights: torch.Tensor
+    masked_m: torch.Tensor
+    expected_m: int
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_status(dev_status: torch.Tensor, where: str = "device") -> None:
+    """Synchronise on the status word and raise MoEError if a kernel reported an error."""
+    v = int(dev_status.item())
+    if v != MOE_OK:
+        raise MoEError(v, where)
+
+
+def new_workspace(num_tokens: int, topk: int, num_experts: int, device=None) -> Optional[torch.Tensor]:
+    n = moe_route_meta_workspace_size(num_tokens, topk, num_experts)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def dispatch_out_shapes(mode: str, quant: str, T: int, H: int, K: int, E: int, M: int):
+    lead = (T * K,) if mode == "normal" else (E, M)
+    if quant == "none":
+        return lead + (H,), torch.bfloat16, None, None
+    if quant == "fp8g128":
+        return lead + (H,), torch.uint8, lead + (H // 128,), torch.float32
+    return lead + (H // 2,), torch.uint8, lead + (H // 16,), torch.uint8
+
+
+def route_meta(topk_ids: torch.Tensor, num_experts: int, num_partitions: int = 1,
+               max_tokens_per_expert: int = 0, workspace: Optional[torch.Tensor] = None,
+               dev_status: Optional[torch.Tensor] = None, stream=None) -> RouteMeta:
+    T, K = topk_ids.shape
+    dev = topk_ids.device
+    seg = torch.empty(num_experts + 1, dtype=torch.int64, device=dev)
+    s2d = torch.empty(T * K, dtype=torch.int32, device=dev)
+    reo = torch.empty(max(T * K, 1), dtype=torch.int32, device=dev)
+    mm = torch.empty(num_experts, dtype=torch.int32, device=dev)
+    pc = torch.empty(num_partitions, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = new_workspace(T, K, num_experts, dev)
+    if dev_status is None:
+        dev_status = new_status(dev)
+    em = moe_route_meta(topk_ids, num_experts, seg, s2d, reo, mm, dev_status, workspace,
+                        num_partitions, max_tokens_per_expert, pc, stream)
+    return RouteMeta(seg, s2d, reo, mm, pc, em)
+
+
+def dispatch(hidden_states: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+             meta: RouteMeta, num_experts: int, mode: str = "normal", quant: str = "none",
+             max_tokens_per_expert: int = 0, input_global_scale: float = 0.0,
+             dev_status: Optional[torch.Tensor] = None, stream=None):
+    T, H = hidden_states.shape
+    K = topk_ids.shape[1]
+    M = max_tokens_per_expert
+    qs, qd, ss, sd = dispatch_out_shapes(mode, quant, T, H, K, num_experts, M)
+    dev = hidden_states.device
+    q = torch.empty(qs, dtype=qd, device=dev)
+    s = torch.empty(ss, dtype=sd, device=dev) if ss is not None else None
+    if dev_status is None:
+        dev_status = new_status(dev)
+    moe_dispatch(mode, quant, hidden_states, topk_ids, num_experts, meta.src2dst, meta.seg_indptr, q, s,
+                 dev_status, M, input_global_scale, stream)
+    if mode == "normal":
+        return NormalDispatchOutput(q, s, topk_ids, topk_weights, meta.seg_indptr, meta.reorder_topk_ids,
+                                    meta.src2dst)
+    return LLDispatchOutput(q, s, topk_ids, topk_weights, meta.masked_m, meta.expected_m)
+
+
+def combine(expert_out: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+            meta: RouteMeta, num_experts: int, mode: str = "normal", max_tokens_per_expert: int = 0,
+            out: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+            stream=None) -> torch.Tensor:
+    T, K = topk_ids.shape
+    H = expert_out.shape[-1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=expert_out.device)
+    if dev_status is None:
+        dev_status = new_status(expert_out.device)
+    moe_combine(mode, expert_out, topk_ids, topk_weights, num_experts, meta.src2dst, meta.seg_indptr,
+                out, dev_status, max_tokens_per_expert, stream)
+    return out
+
+
+class MoEDispatcher:
+    """Pre-allocated buffers for repeated dispatch/combine of one shape (graph-capturable).
+
+    Every launch goes to the current torch stream (or ``stream``); no call allocates
+    after construction, so the three launches can be captured in a CUDA graph.
+    """
+
+    def __init__(self, num_tokens: int, hidden: int, topk: int, num_experts: int, *, mode: str = "normal",
+                 quant: str = "none", num_partitions: int = 1, max_tokens_per_expert: int = 0,
+                 device=None):
+        self.T, self.H, self.K, self.E = num_tokens, hidden, topk, num_experts
+        self.mode, self.quant, self.P, self.M = mode, quant, num_partitions, max_tokens_per_expert
+        dev = torch.device(device or "cuda")
+        T, K, E = num_tokens, topk, num_experts
+        self.status = new_status(dev)
+        self.workspace = new_workspace(T, K, E, dev)
+        self.seg_indptr = torch.zeros(E + 1, dtype=torch.int64, device=dev)
+        self.src2dst = torch.empty(max(T * K, 1), dtype=torch.int32, device=dev)
+        self.reorder_topk_ids = torch.empty(max(T * K, 1), dtype=torch.int32, device=dev)
+        self.masked_m = torch.zeros(E, dtype=torch.int32, device=dev)
+        self.partition_counts = torch.zeros(num_partitions, dtype=torch.int32, device=dev)
+        qs, qd, ss, sd = dispatch_out_shapes(mode, quant, T, hidden, K, E, max_tokens_per_expert)
+        self.out_q = torch.empty(qs, dtype=qd, device=dev)
+        self.out_scales = torch.empty(ss, dtype=sd, device=dev) if ss is not None else None
+        self.out = torch.empty((T, hidden), dtype=torch.bfloat16, device=dev)
+        self.expected_m = (T * K + E) // E
+
+    def route(self, topk_ids: torch.Tensor, stream=None) -> int:
+        self.expected_m = moe_route_meta(topk_ids, self.E, self.seg_indptr, self.src2dst, self.reorder_topk_ids,
+                                         self.masked_m, self.status, self.workspace, self.P, self.M,
+                                         self.partition_counts, stream)
+        return self.expected_m
+
+    def dispatch(self, hidden_states: torch.Tensor, topk_ids: torch.Tensor, input_global_scale: float = 0.0,
+                 stream=None) -> None:
+        moe_dispatch(self.mode, self.quant, hidden_states, topk_ids, self.E, self.src2dst, self.seg_indptr,
+                     self.out_q, self.out_scales, self.status, self.M, input_global_scale, stream)
+
+    def combine(self, expert_out: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                stream=None) -> torch.Tensor:
+        moe_combine(self.mode, expert_out, topk_ids, topk_weights, self.E, self.src2dst, self.seg_indptr,
+                    self.out, self.status, self.M, stream)
+        return self.out
+
+    def check(self) -> None:
+        check_status(self.status, "MoEDispatcher")

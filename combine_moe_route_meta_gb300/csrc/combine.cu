@@ -1,0 +1,176 @@
+// combine.cu -- weighted reduction of expert outputs back to token order.
+//
+// Operation (deepep_post_reorder in combine_a, "sglang 0.4.4.post2 -> 0.4.4.post4,
+// ep_moe/token_dispatcher.py" diff; low_latency_combine in
+// _DeepEPDispatcherImplLowLatency._combine_core, "sglang token_dispatcher/deepep.py" page):
+//   out[t, :] = bf16_rn( sum_{k valid, ascending} topk_weights[t,k] * expert_out[row(t,k), :] )
+// row = src2dst (normal) or e*M + rank (masked); fp32 fused multiply-add accumulation.
+//
+// Design: HBM-bound K-way gather. One warp per (token, 512-column slice); each lane owns
+// 16 columns. Lanes 0..K-1 fetch the slot metadata (row, weight) and broadcast it by
+// shuffle; each lane then issues the loads of up to 8 source rows (2 x 16 B per row,
+// ld.global.nc with L1::no_allocate) before consuming any, so a warp keeps 8 KB in
+// flight. Accumulation order is fixed (k ascending) and the result is rounded once to
+// bf16 (cvt.rn.bf16x2). A token with no valid slot gets zeros.
+#include <cstdint>
+
+#include "moe_device.cuh"
+#include "moe_launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kCombineThreads = 256;
+constexpr int kSlice = 512;
+constexpr int kLaneElems = 16;
+constexpr int kBatch = 8;  // source rows in flight per lane
+
+struct CombineArgs {
+    const uint16_t* eo;
+    int64_t T;
+    int H, K, E, M;
+    const int32_t* ids;
+    const int32_t* src2dst;
+    const int64_t* seg;
+    const float* w;
+    uint16_t* out;
+    int32_t* status;
+    int units_per_row;
+    int64_t n_units;
+    int64_t max_row;
+};
+
+template <bool MASKED>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int H = a.H;
+
+    for (int64_t u = warp; u < a.n_units; u += nwarps) {
+        const int64_t t = u / a.units_per_row;
+        const int col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
+        const bool active = col < H;
+
+        int64_t my_row = -1;
+        float my_w = 0.0f;
+        if (lane < a.K) {
+            const int64_t i = t * a.K + lane;
+            const int d = __ldg(a.src2dst + i);
+            my_w = __ldg(a.w + i);
+            if (d >= 0) {
+                if (MASKED) {
+                    const int e = __ldg(a.ids + i);
+                    if (e >= 0 && e < a.E) {
+                        const int64_t rank = int64_t(d) - __ldg(a.seg + e);
+                        if (rank >= 0 && rank < a.M) my_row = int64_t(e) * a.M + rank;
+                    } else {
+                        set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
+                    }
+                } else if (d < a.max_row) {
+                    my_row = d;
+                } else {
+                    set_status(a.status, MOE_ERR_INVALID_ARG);
+                }
+            }
+        }
+
+        float acc[kLaneElems];
+#pragma unroll
+        for (int j = 0; j < kLaneElems; j++) acc[j] = 0.0f;
+
+        for (int k0 = 0; k0 < a.K; k0 += kBatch) {
+            int64_t rows[kBatch];
+            float wk[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                const int k = k0 + j;
+                rows[j] = __shfl_sync(kFullMask, my_row, k & 31);
+                wk[j] = __shfl_sync(kFullMask, my_w, k & 31);
+                if (k >= a.K || !active) rows[j] = -1;
+            }
+            uint4 v[kBatch][2];
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                if (rows[j] >= 0) {
+                    const uint16_t* p = a.eo + rows[j] * H + col;
+                    v[j][0] = ld_stream_v4(p);
+                    v[j][1] = ld_stream_v4(p + 8);
+                } else {
+                    v[j][0] = make_uint4(0, 0, 0, 0);
+                    v[j][1] = v[j][0];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                if (rows[j] >= 0) {
+                    float f[16];
+                    unpack8(v[j][0], f);
+                    unpack8(v[j][1], f + 8);
+#pragma unroll
+                    for (int e = 0; e < kLaneElems; e++) acc[e] = fmaf(wk[j], f[e], acc[e]);
+                }
+            }
+        }
+        if (active) {
+            uint16_t* dst = a.out + t * H + col;
+            st_v4(dst, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+            st_v4(dst + 8, make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                      pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
+        }
+    }
+}
+
+template <bool MASKED>
+cudaError_t launch_variant(const LaunchCtx& ctx, const CombineArgs& a) {
+    auto kern = combine_kernel<MASKED>;
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCombineThreads, 0);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t warps_per_block = kCombineThreads / 32;
+    const int64_t need = (a.n_units + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = int64_t(ctx.num_sms) * per_sm;
+    const int grid = int(need < cap ? need : cap);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const LaunchCtx& ctx, int mode, const uint16_t* expert_out, int64_t T,
+                           int H, int K, int E, int M, const int32_t* topk_ids,
+                           const int32_t* src2dst, const int64_t* seg_indptr,
+                           const float* topk_weights, uint16_t* out, int32_t* dev_status) {
+    CombineArgs a{};
+    a.eo = expert_out;
+    a.T = T;
+    a.H = H;
+    a.K = K;
+    a.E = E;
+    a.M = M;
+    a.ids = topk_ids;
+    a.src2dst = src2dst;
+    a.seg = seg_indptr;
+    a.w = topk_weights;
+    a.out = out;
+    a.status = dev_status;
+    a.units_per_row = (H + kSlice - 1) / kSlice;
+    a.n_units = T * a.units_per_row;
+    a.max_row = T * K;
+    return mode == MOE_MODE_MASKED ? launch_variant<true>(ctx, a) : launch_variant<false>(ctx, a);
+}
+
+}  // namespace moe

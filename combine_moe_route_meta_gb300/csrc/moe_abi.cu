@@ -1,0 +1,161 @@
+// moe_abi.cu -- the extern "C" entry points declared in include/moe_dispatch.h.
+//
+// Each entry point validates its arguments on the host (returning a status and launching
+// nothing on failure), reads the SM count of the current device, and hands the launch to
+// the kernel files. The library allocates no memory and keeps no state between calls.
+#include <climits>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_dispatch.h"
+#include "moe_launch.h"
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+moe_status_t make_ctx(moe_stream_t stream, moe::LaunchCtx* ctx) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    ctx->stream = reinterpret_cast<cudaStream_t>(stream);
+    ctx->num_sms = sms > 0 ? sms : 1;
+    return MOE_OK;
+}
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// shared checks of (T, K, E)
+moe_status_t check_shape(int64_t T, int K, int E) {
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (K < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+    if (K > MOE_MAX_TOPK || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && T > int64_t(INT32_MAX) / K) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument (size, null or misaligned pointer)";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: size beyond the library's limits";
+        case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY: an expert received more than max_tokens_per_expert pairs";
+        case MOE_ERR_BAD_EXPERT_ID: return "MOE_ERR_BAD_EXPERT_ID: an expert id outside [-1, num_experts) was skipped";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait gave up";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA runtime call or launch failed";
+        default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+size_t moe_route_meta_workspace_size(int64_t num_tokens, int topk, int num_experts) {
+    if (check_shape(num_tokens, topk, num_experts) != MOE_OK) return 0;
+    return moe::plan_route_meta(num_tokens * topk, num_experts).ws_bytes;
+}
+
+moe_status_t moe_route_meta(const int32_t* topk_ids, int64_t num_tokens, int topk, int num_experts,
+                            int num_partitions, int max_tokens_per_expert, int64_t* seg_indptr,
+                            int32_t* src2dst, int32_t* reorder_topk_ids, int32_t* masked_m,
+                            int32_t* partition_counts, int32_t* expected_m_host, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+    moe_status_t st = check_shape(num_tokens, topk, num_experts);
+    if (st != MOE_OK) return st;
+    if (num_partitions < 1 || num_experts % num_partitions != 0) return MOE_ERR_INVALID_ARG;
+    if (max_tokens_per_expert < 0) return MOE_ERR_INVALID_ARG;
+    if (!seg_indptr || !masked_m || !dev_status) return MOE_ERR_INVALID_ARG;
+    const int64_t n_pairs = num_tokens * topk;
+    if (n_pairs > 0 && (!topk_ids || !src2dst || !reorder_topk_ids)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(seg_indptr, 8) || !aligned(topk_ids, 4) || !aligned(src2dst, 4) ||
+        !aligned(reorder_topk_ids, 4) || !aligned(masked_m, 4) || !aligned(partition_counts, 4) ||
+        !aligned(dev_status, 4))
+        return MOE_ERR_INVALID_ARG;
+    const moe::RoutePlan plan = moe::plan_route_meta(n_pairs, num_experts);
+    if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)))
+        return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    if (expected_m_host) *expected_m_host = int32_t((n_pairs + num_experts) / num_experts);
+    return from_cuda(moe::launch_route_meta(ctx, plan, topk_ids, n_pairs, topk, num_experts,
+                                            num_partitions, max_tokens_per_expert, seg_indptr,
+                                            src2dst, reorder_topk_ids, masked_m, partition_counts,
+                                            workspace, dev_status));
+}
+
+moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t* hidden_states,
+                          int64_t num_tokens, int hidden, const int32_t* topk_ids, int topk,
+                          int num_experts, int max_tokens_per_expert, const int32_t* src2dst,
+                          const int64_t* seg_indptr, float input_global_scale, void* out_q,
+                          void* out_scales, int32_t* dev_status, moe_stream_t stream) {
+    if (mode != MOE_MODE_NORMAL && mode != MOE_MODE_MASKED) return MOE_ERR_INVALID_ARG;
+    if (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_G128 && quant != MOE_QUANT_NVFP4_B16)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(num_tokens, topk, num_experts);
+    if (st != MOE_OK) return st;
+    if (hidden <= 0 || hidden % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (quant == MOE_QUANT_FP8_G128 && hidden % 128 != 0) return MOE_ERR_INVALID_ARG;
+    const bool masked = mode == MOE_MODE_MASKED;
+    if (masked && max_tokens_per_expert < 1) return MOE_ERR_INVALID_ARG;
+    if (!dev_status) return MOE_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MOE_OK;
+    if (!hidden_states || !src2dst || !out_q) return MOE_ERR_INVALID_ARG;
+    if (masked && (!topk_ids || !seg_indptr)) return MOE_ERR_INVALID_ARG;
+    if (quant != MOE_QUANT_NONE && !out_scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(hidden_states, 16) || !aligned(out_q, 16) || !aligned(src2dst, 4) ||
+        !aligned(topk_ids, 4) || !aligned(seg_indptr, 8) || !aligned(dev_status, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (quant == MOE_QUANT_FP8_G128 && !aligned(out_scales, 4)) return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_dispatch(ctx, int(mode), int(quant), hidden_states, num_tokens,
+                                          hidden, topk_ids, topk, num_experts,
+                                          masked ? max_tokens_per_expert : 0, src2dst, seg_indptr,
+                                          input_global_scale, out_q, out_scales, dev_status));
+}
+
+moe_status_t moe_combine(moe_mode_t mode, const uint16_t* expert_out, int64_t num_tokens, int hidden,
+                         int topk, int num_experts, int max_tokens_per_expert,
+                         const int32_t* topk_ids, const int32_t* src2dst, const int64_t* seg_indptr,
+                         const float* topk_weights, uint16_t* out, int32_t* dev_status,
+                         moe_stream_t stream) {
+    if (mode != MOE_MODE_NORMAL && mode != MOE_MODE_MASKED) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(num_tokens, topk, num_experts);
+    if (st != MOE_OK) return st;
+    if (hidden <= 0 || hidden % 16 != 0) return MOE_ERR_INVALID_ARG;
+    const bool masked = mode == MOE_MODE_MASKED;
+    if (masked && max_tokens_per_expert < 1) return MOE_ERR_INVALID_ARG;
+    if (!dev_status) return MOE_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MOE_OK;
+    if (!expert_out || !src2dst || !topk_weights || !out) return MOE_ERR_INVALID_ARG;
+    if (masked && (!topk_ids || !seg_indptr)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_out, 16) || !aligned(out, 16) || !aligned(src2dst, 4) ||
+        !aligned(topk_ids, 4) || !aligned(seg_indptr, 8) || !aligned(topk_weights, 4) ||
+        !aligned(dev_status, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_combine(ctx, int(mode), expert_out, num_tokens, hidden, topk,
+                                         num_experts, masked ? max_tokens_per_expert : 0, topk_ids,
+                                         src2dst, seg_indptr, topk_weights, out, dev_status));
+}
+
+moe_status_t moe_convert_probe(const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1,
+                               float* e4m3_value, moe_stream_t stream) {
+    if (n < 0 || n % 2 != 0) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!in || !aligned(in, 8) || !aligned(e4m3_value, 4)) return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    moe_status_t st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_convert_probe(ctx, in, n, e4m3, e2m1, e4m3_value));
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// moe_device.cuh -- device helpers shared by the route-meta, dispatch and combine kernels.
+//
+// Everything here is written for sm_103a. The number-format conversions use the
+// hardware cvt instructions (round-to-nearest-even, satfinite); the library's GPU
+// tests compare them exhaustively on their decision points against an independent
+// CPU implementation of the formats.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "moe_dispatch.h"
+
+namespace moe {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// status word: first error wins
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+    if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), MOE_OK, code);
+}
+
+// ---------------------------------------------------------------------------
+// memory access with cache hints
+// ---------------------------------------------------------------------------
+// 16-byte read-only load that does not allocate in L1 (each byte is read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// two fp32 -> packed bf16x2, round-to-nearest-even; `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// unpack 8 bf16 (one uint4) into fp32
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 / FP4 E2M1 conversions (hardware cvt, RNE, satfinite)
+// ---------------------------------------------------------------------------
+// two fp32 -> two e4m3 codes in one 16-bit word; `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// two fp32 -> two e2m1 codes in one byte; `lo` lands in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 t;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+        "cvt.u32.u8 %0, t;\n\t}"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// exact value of an e4m3 code (through f16, which holds every e4m3 value exactly)
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    uint32_t h2;
+    uint16_t c = static_cast<uint16_t>(code & 0xffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Wait until the kernels this launch depends on have completed and flushed memory.
+// A no-op when the kernel was not launched as a programmatic dependent.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream to begin launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+}  // namespace moe

@@ -1,0 +1,217 @@
+/*
+ * moe_dispatch.h -- C ABI of the GB300 (sm_103a) MoE token dispatch / combine library.
+ *
+ * Three stream-ordered calls cover the hot path of the SGLang dispatcher pages:
+ *
+ *   moe_route_meta  top-k routing -> per-expert metadata (histogram, exclusive scan,
+ *                   stable per-pair rank): seg_indptr, src2dst, reorder_topk_ids,
+ *                   masked_m. This is deepep_run_moe_deep_preprocess as consumed by
+ *                   _DeepEPDispatcherImplNormal._deepep_permute ("sglang 0.4.4.post2 ->
+ *                   0.4.4.post4, ep_moe/token_dispatcher.py" diff), plus the
+ *                   low-latency counts of _DeepEPDispatcherImplLowLatency.dispatch_a
+ *                   ("sglang token_dispatcher/deepep.py" page).
+ *   moe_dispatch    gathers token rows into the expert-contiguous layout [N, .]
+ *                   (the PreReorder permute) or into the low-latency masked layout
+ *                   [E, M, .] (low_latency_dispatch), optionally fused with FP8 e4m3
+ *                   per-token-group-128 quantisation (sglang_per_token_group_quant_fp8,
+ *                   deepep.py page, _DeepEPDispatcherImplNormal.dispatch_a) or NVFP4
+ *                   block-16 quantisation (fp4_quantize, "sglang
+ *                   token_dispatcher/flashinfer.py" page, FlashinferDispatcher.dispatch).
+ *   moe_combine     topk_weights-weighted, fp32-accumulated reduction of expert outputs
+ *                   back to token order (deepep_post_reorder on the diff page,
+ *                   low_latency_combine on the deepep.py page).
+ *
+ * Conventions (all calls):
+ *  - Every pointer argument is a DEVICE pointer unless its name ends in _host.
+ *    The caller allocates and owns every buffer, including the workspace; the
+ *    library keeps no pointer after a call returns.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
+ *    never synchronise the host.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    returned as a moe_status_t; nothing is written in that case.
+ *  - Data-dependent errors are written by the kernels into the caller's device word
+ *    *dev_status, first error wins (atomic compare-and-swap from MOE_OK). The caller
+ *    sets *dev_status = 0 before use and reads it whenever it chooses; the kernels
+ *    never trap, never assert and never spin without a bound.
+ *  - bf16 tensors are passed as their 16-bit patterns (uint16_t), row-major.
+ *  - Notation: T tokens, H hidden size, K top-k slots per token, E experts,
+ *    M = num_max_dispatch_tokens_per_rank (slots per expert in the masked layout),
+ *    pair i = t*K + k, a pair is valid iff 0 <= topk_ids[i] < E, N = #valid pairs.
+ */
+#ifndef MOE_DISPATCH_H
+#define MOE_DISPATCH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL selects the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* host-side: bad size, null or misaligned pointer     */
+    MOE_ERR_UNSUPPORTED = 2,    /* host-side: a size beyond the limits below           */
+    MOE_ERR_CAPACITY = 3,       /* device: an expert received more than M pairs        */
+    MOE_ERR_BAD_EXPERT_ID = 4,  /* device: an id outside [-1, E) was seen (skipped)    */
+    MOE_ERR_TIMEOUT = 5,        /* device: a bounded wait gave up                      */
+    MOE_ERR_CUDA = 6            /* host-side: a CUDA launch or runtime call failed     */
+} moe_status_t;
+
+typedef enum { MOE_MODE_NORMAL = 0, MOE_MODE_MASKED = 1 } moe_mode_t;
+
+typedef enum {
+    MOE_QUANT_NONE = 0,        /* bf16 rows                                                  */
+    MOE_QUANT_FP8_G128 = 1,    /* e4m3 rows [.., H] + fp32 scales [.., H/128]                */
+    MOE_QUANT_NVFP4_B16 = 2    /* e2m1 rows [.., H/2] (2 per byte) + e4m3 scales [.., H/16]  */
+} moe_quant_t;
+
+#define MOE_MAX_EXPERTS 1024   /* E <= 1024                                  */
+#define MOE_MAX_TOPK 16        /* 1 <= K <= 16                               */
+#define MOE_ABI_VERSION 1
+
+/* Version of this ABI (MOE_ABI_VERSION of the built library). */
+int moe_abi_version(void);
+
+/* Human-readable name of a status code; never NULL. */
+const char *moe_status_string(moe_status_t status);
+
+/*
+ * Bytes of scratch that moe_route_meta needs for num_tokens x topk pairs and
+ * num_experts experts (0 when one thread block handles all pairs). The workspace
+ * must be zero-filled once when it is allocated; every call that completes leaves
+ * it ready for the next call. Returns 0 for arguments moe_route_meta would reject.
+ */
+size_t moe_route_meta_workspace_size(int64_t num_tokens, int topk, int num_experts);
+
+/*
+ * moe_route_meta -- routing metadata: histogram, exclusive scan, stable rank.
+ *
+ * Operation (deepep_run_moe_deep_preprocess as used by _deepep_permute on the diff
+ * page; masked_m / expected_m as in _DeepEPDispatcherImplLowLatency.dispatch_a on the
+ * deepep.py page; invalid slots marked -1 as noted in DeepEPDispatcher.__init__):
+ *   count[e]       = #{i valid : topk_ids[i] = e}
+ *   seg_indptr[0]  = 0,  seg_indptr[e+1] = seg_indptr[e] + count[e]
+ *   src2dst[i]     = seg_indptr[id_i] + #{j < i valid : id_j = id_i}, or -1 if invalid
+ *   reorder_topk_ids[src2dst[i]] = id_i            (first N entries, non-decreasing)
+ *   masked_m[e]    = count[e] if M == 0, else min(count[e], M)
+ *   partition_counts[p] = seg_indptr[(p+1)*E/P] - seg_indptr[p*E/P]
+ *   *expected_m_host = (T*K + E) / E                (host value, computed without a sync)
+ *
+ * Arguments:
+ *   topk_ids            [T, K] int32, row-major. -1 = empty slot (skipped silently);
+ *                       any other id outside [0, E) is skipped and reported as
+ *                       MOE_ERR_BAD_EXPERT_ID in *dev_status.
+ *   num_tokens (T)      >= 0; T*K <= INT32_MAX. T = 0 is legal (outputs zeroed).
+ *   topk (K)            1..MOE_MAX_TOPK.
+ *   num_experts (E)     1..MOE_MAX_EXPERTS.
+ *   num_partitions (P)  >= 1, E % P == 0 (logical expert-parallel ranks of E/P experts).
+ *   max_tokens_per_expert (M)  >= 0. M > 0 enables the capacity check: an expert with
+ *                       more than M pairs sets MOE_ERR_CAPACITY; its extra pairs keep
+ *                       their src2dst but land in no masked slot.
+ *   seg_indptr          [E+1] int64 out.
+ *   src2dst             [T*K] int32 out.
+ *   reorder_topk_ids    [T*K] int32 out (capacity; the first N entries are written).
+ *   masked_m            [E] int32 out.
+ *   partition_counts    [P] int32 out, or NULL.
+ *   expected_m_host     host int32 out, or NULL.
+ *   workspace           moe_route_meta_workspace_size(T, K, E) bytes, zero-filled at
+ *                       allocation; may be NULL when that size is 0.
+ *   dev_status          [1] int32 device status word (see conventions).
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
+ */
+moe_status_t moe_route_meta(const int32_t *topk_ids, int64_t num_tokens, int topk,
+                            int num_experts, int num_partitions, int max_tokens_per_expert,
+                            int64_t *seg_indptr, int32_t *src2dst, int32_t *reorder_topk_ids,
+                            int32_t *masked_m, int32_t *partition_counts,
+                            int32_t *expected_m_host, void *workspace, size_t workspace_bytes,
+                            int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_dispatch -- gather (and optionally quantise) token rows into expert order.
+ *
+ * Operation (the PreReorder permute of _deepep_permute on the diff page; the masked
+ * layout of low_latency_dispatch on the deepep.py page):
+ *   normal: row r = src2dst[i]                            of out [T*K (capacity N), .]
+ *   masked: row r = e*M + (src2dst[i] - seg_indptr[e])    of out [E, M, .], e = topk_ids[i];
+ *           pairs with rank >= M are dropped (moe_route_meta reported them).
+ *   out[r] = Q(hidden_states[t]) for every valid pair i = t*K + k. Rows no pair maps
+ *   to (rows >= N, masked slots >= masked_m[e]) are left untouched.
+ *   Q = identity (MOE_QUANT_NONE), or per group of 128 consecutive elements
+ *   (MOE_QUANT_FP8_G128):  amax = max|x|, s = max(amax, 1e-10) / 448,
+ *       q = e4m3_rn_satfinite(x / s), scale = s (fp32);
+ *   or per block of 16 consecutive elements with g = input_global_scale
+ *   (MOE_QUANT_NVFP4_B16):  sf = e4m3_rn_satfinite((amax / 6) * g),
+ *       q = e2m1_rn_satfinite(x * (g / sf)), all codes 0 when sf decodes to 0;
+ *       two codes per byte, the even element in the low nibble; sf row-major [H/16].
+ *   All arithmetic is binary32 with round-to-nearest-even, in the order written.
+ *
+ * Arguments:
+ *   hidden_states  [T, H] bf16, 16-byte aligned.
+ *   hidden (H)     > 0, H % 16 == 0; H % 128 == 0 for MOE_QUANT_FP8_G128.
+ *   topk_ids       [T, K] int32 (read in masked mode; may be NULL in normal mode).
+ *   max_tokens_per_expert (M)  >= 1 in masked mode; ignored in normal mode.
+ *   src2dst        [T*K] int32 and seg_indptr [E+1] int64 from moe_route_meta
+ *                  (seg_indptr is read in masked mode only; may be NULL otherwise).
+ *   out_q          rows as above, 16-byte aligned. bf16 rows hold H uint16, FP8 rows
+ *                  H bytes, NVFP4 rows H/2 bytes.
+ *   out_scales     FP8: fp32 [rows, H/128] (4-byte aligned); NVFP4: uint8 [rows, H/16];
+ *                  NULL for MOE_QUANT_NONE.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
+ */
+moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t *hidden_states,
+                          int64_t num_tokens, int hidden, const int32_t *topk_ids, int topk,
+                          int num_experts, int max_tokens_per_expert, const int32_t *src2dst,
+                          const int64_t *seg_indptr, float input_global_scale, void *out_q,
+                          void *out_scales, int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_combine -- weighted reduction of expert outputs back to token order.
+ *
+ * Operation (deepep_post_reorder in combine_a on the diff page; low_latency_combine in
+ * _DeepEPDispatcherImplLowLatency._combine_core on the deepep.py page):
+ *   out[t, :] = bf16_rn( sum_{k valid, k ascending} topk_weights[t, k] * expert_out[row(t,k), :] )
+ *   with row as in moe_dispatch; fp32 fused multiply-add accumulation. A token with
+ *   no valid slot gets zeros.
+ *
+ * Arguments:
+ *   expert_out     bf16 [N (capacity T*K), H] (normal) or [E, M, H] (masked), 16-byte aligned.
+ *   topk_ids       [T, K] int32 (read in masked mode; may be NULL in normal mode).
+ *   src2dst, seg_indptr  from moe_route_meta (seg_indptr read in masked mode only).
+ *   topk_weights   [T, K] fp32.
+ *   out            [T, H] bf16 out, 16-byte aligned, must not overlap expert_out.
+ *   hidden (H)     > 0, H % 16 == 0.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
+ */
+moe_status_t moe_combine(moe_mode_t mode, const uint16_t *expert_out, int64_t num_tokens,
+                         int hidden, int topk, int num_experts, int max_tokens_per_expert,
+                         const int32_t *topk_ids, const int32_t *src2dst,
+                         const int64_t *seg_indptr, const float *topk_weights, uint16_t *out,
+                         int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_convert_probe -- diagnostics: run the number-format conversions of the quantising
+ * kernels on arbitrary fp32 inputs, so their rounding, saturation, signed zeros and
+ * packing order can be checked against an independent implementation of the formats.
+ * (No counterpart on the pages: a test hook for the e4m3 / e2m1 codecs used by
+ * sglang_per_token_group_quant_fp8 and fp4_quantize.)
+ *   in          [n] fp32, n even.
+ *   e4m3        [n] uint8 out: e4m3_rn_satfinite(in[j]), converted in pairs
+ *               (in[2j], in[2j+1]) exactly as the FP8 kernel packs them; or NULL.
+ *   e2m1        [n/2] uint8 out: byte j = e2m1(in[2j]) | e2m1(in[2j+1]) << 4, as the NVFP4
+ *               kernel packs them; or NULL.
+ *   e4m3_value  [n] fp32 out: the value of the e4m3 code of in[j], decoded as the NVFP4
+ *               kernel decodes its block scales; or NULL.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
+ */
+moe_status_t moe_convert_probe(const float *in, int64_t n, uint8_t *e4m3, uint8_t *e2m1,
+                               float *e4m3_value, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DISPATCH_H */

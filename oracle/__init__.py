@@ -64,6 +64,8 @@ def _load():
             "oracle_e4m3_from_float": (ctypes.c_uint8, [f32]),
             "oracle_e2m1_to_double": (ctypes.c_double, [ctypes.c_uint8]),
             "oracle_e2m1_from_float": (ctypes.c_uint8, [f32]),
+            "oracle_e4m3_from_float_array": (None, [P, i64, P]),
+            "oracle_e2m1_from_float_array": (None, [P, i64, P]),
             "oracle_route_meta": (ctypes.c_int, [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, P, P, P, P, P]),
             "oracle_expected_m": (i64, [i64, ctypes.c_int, ctypes.c_int]),
@@ -108,6 +110,20 @@ def e2m1_from_float(v: float) -> int:
 
 def e2m1_to_float(c: int) -> float:
     return float(_load().oracle_e2m1_to_double(int(c)))
+
+
+def e4m3_from_float_array(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.size, np.uint8)
+    _load().oracle_e4m3_from_float_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def e2m1_from_float_array(v: np.ndarray) -> np.ndarray:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.empty(v.size, np.uint8)
+    _load().oracle_e2m1_from_float_array(_ptr(v), v.size, _ptr(out))
+    return out
 
 
 def bf16_from_double(v: float) -> int:

@@ -165,6 +165,17 @@ uint8_t oracle_e2m1_from_float(float v)
     return (uint8_t)(sign | (uint8_t)code);
 }
 
+/* array forms of the encoders, for comparing many values at once */
+void oracle_e4m3_from_float_array(const float *v, int64_t n, uint8_t *out)
+{
+    for (int64_t j = 0; j < n; j++) out[j] = oracle_e4m3_from_float(v[j]);
+}
+
+void oracle_e2m1_from_float_array(const float *v, int64_t n, uint8_t *out)
+{
+    for (int64_t j = 0; j < n; j++) out[j] = oracle_e2m1_from_float(v[j]);
+}
+
 /* ------------------------------------------------------------------------- */
 /* step a1-a3: routing metadata                                               */
 /* ------------------------------------------------------------------------- */

@@ -1,0 +1,205 @@
+"""Test harness: runs one seeded workload through the CUDA library (via the C ABI
+binding) and through the CPU oracle, and compares them.
+
+Bars (the method's own): bit-exact for the metadata, the gathered bf16 rows and the
+quantised bytes/scales; the combine within 1e-2 relative / 1e-3 absolute of the
+oracle's binary64 sum rounded to bf16 (elementwise |gpu - oracle| <= 1e-3 + 1e-2*|oracle|).
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+import oracle
+from workloads import Workload, bf16_bits_to_f32, random_bf16
+
+RTOL = 1e-2
+ATOL = 1e-3
+SENTINEL = 0xA5
+
+STATUS_OF_ORACLE = {0: {0}, oracle.BAD_ID: {4}, oracle.CAPACITY: {3}, oracle.BAD_ID | oracle.CAPACITY: {3, 4}}
+
+
+def moe():
+    import combine_moe_route_meta_gb300 as m
+    return m
+
+
+def to_dev(w: Workload):
+    x = torch.from_numpy(np.ascontiguousarray(w.x).view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.from_numpy(np.ascontiguousarray(w.topk_ids)).cuda()
+    wt = torch.from_numpy(np.ascontiguousarray(w.topk_weights)).cuda()
+    return x, ids, wt
+
+
+def bytes_of(t: torch.Tensor) -> np.ndarray:
+    """Host copy of a device tensor's raw bytes, shaped [rows, row_bytes]."""
+    rows = t.shape[0] if t.dim() > 1 else 1
+    a = t.contiguous().view(torch.uint8).cpu().numpy()
+    width = a.size // rows if rows else 0
+    return a.reshape(rows, width)
+
+
+def filled(shape, dtype, fill=SENTINEL) -> torch.Tensor:
+    n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+    return torch.full((n,), fill, dtype=torch.uint8, device="cuda").view(dtype).view(shape)
+
+
+def check_meta(w: Workload, om: oracle.Meta, gm, status: torch.Tensor):
+    n = om.num_valid
+    assert np.array_equal(gm.seg_indptr.cpu().numpy(), om.seg_indptr), "seg_indptr"
+    assert np.array_equal(gm.src2dst.cpu().numpy(), om.src2dst), "src2dst"
+    assert np.array_equal(gm.reorder_topk_ids[:n].cpu().numpy(), om.reorder_topk_ids), "reorder_topk_ids"
+    assert np.array_equal(gm.masked_m.cpu().numpy(), om.masked_m), "masked_m"
+    assert np.array_equal(gm.partition_counts.cpu().numpy(), om.partition_counts), "partition_counts"
+    assert gm.expected_m == om.expected_m
+    assert int(status.item()) in STATUS_OF_ORACLE[om.status], (int(status.item()), om.status)
+
+
+def gpu_meta(w: Workload, ids: torch.Tensor):
+    m = moe()
+    status = m.new_status()
+    gm = m.route_meta(ids, w.E, num_partitions=w.P, max_tokens_per_expert=w.M, dev_status=status)
+    return gm, status
+
+
+def check_combine(got_bits: np.ndarray, want_bits: np.ndarray, what="combine"):
+    g = bf16_bits_to_f32(got_bits).astype(np.float64)
+    o = bf16_bits_to_f32(want_bits).astype(np.float64)
+    err = np.abs(g - o)
+    bad = err > ATOL + RTOL * np.abs(o)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements out of tolerance, max err {err.max()}"
+
+
+def masked_rows(w: Workload, om: oracle.Meta):
+    """Masked-layout row of every valid pair (flattened pair order), -1 where dropped/invalid."""
+    flat = w.topk_ids.reshape(-1)
+    rows = np.full(flat.size, -1, np.int64)
+    v = om.src2dst >= 0
+    e = flat[v].astype(np.int64)
+    rank = om.src2dst[v].astype(np.int64) - om.seg_indptr[e]
+    r = np.where(rank < w.M, e * w.M + rank, -1)
+    rows[np.nonzero(v)[0]] = r
+    return rows
+
+
+def run_full(w: Workload, *, expert_seed: int = 1234, check_untouched: bool = True):
+    """Meta + dispatch + combine on the GPU, each compared in full with the oracle."""
+    m = moe()
+    x, ids, wt = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, w.E, P=w.P, M=w.M)
+    gm, status = gpu_meta(w, ids)
+    torch.cuda.synchronize()
+    check_meta(w, om, gm, status)
+
+    # ---- dispatch ----
+    qs, qd, ss, sd = m.dispatch_out_shapes(w.mode, w.quant, w.T, w.H, w.K, w.E, w.M)
+    q = filled(qs, qd)
+    s = filled(ss, sd) if ss is not None else None
+    st2 = m.new_status()
+    if w.T:
+        m.moe_dispatch(w.mode, w.quant, x, ids, w.E, gm.src2dst, gm.seg_indptr, q, s, st2, w.M,
+                       w.global_scale or 0.0)
+    oq, osc = oracle.dispatch(w.mode, w.quant, w.x, w.topk_ids, om, w.E, M=w.M,
+                              global_scale=w.global_scale or 0.0, fill=SENTINEL)
+    torch.cuda.synchronize()
+    gq = bytes_of(q)
+    oqb = np.ascontiguousarray(oq).view(np.uint8).reshape(gq.shape)
+    if check_untouched:
+        assert np.array_equal(gq, oqb), "dispatch rows (incl. untouched sentinel rows)"
+    else:
+        n = om.num_valid
+        assert np.array_equal(gq[:n], oqb[:n])
+    if s is not None:
+        gs = bytes_of(s)
+        osb = np.ascontiguousarray(osc).view(np.uint8).reshape(gs.shape)
+        assert np.array_equal(gs, osb), "dispatch scales"
+    assert int(st2.item()) == 0
+
+    # ---- combine ----
+    rng = np.random.default_rng(expert_seed)
+    if w.mode == "normal":
+        eo_host = random_bf16(rng, (max(w.T * w.K, 1), w.H))
+    else:
+        eo_host = random_bf16(rng, (w.E * w.M, w.H))
+    eo = torch.from_numpy(eo_host.view(np.int16)).cuda().view(torch.bfloat16)
+    out = filled((w.T, w.H), torch.bfloat16)
+    st3 = m.new_status()
+    if w.T:
+        m.moe_combine(w.mode, eo, ids, wt, w.E, gm.src2dst, gm.seg_indptr, out, st3, w.M)
+    want = oracle.combine(w.mode, eo_host, w.topk_ids, w.topk_weights, om, w.E, M=w.M)
+    torch.cuda.synchronize()
+    check_combine(bytes_of(out).view(np.uint16).reshape(w.T, w.H), want)
+    assert int(st3.item()) == 0
+    return om
+
+
+def run_sampled(w: Workload, *, n_sample: int = 256, expert_seed: int = 4321, sample_seed: int = 7):
+    """Full-size workload in the benchmark's launch configuration: metadata compared in full,
+    dispatch and combine compared on a seeded sample of tokens (all K rows of each)."""
+    m = moe()
+    x, ids, wt = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, w.E, P=w.P, M=w.M)
+    gm, status = gpu_meta(w, ids)
+    torch.cuda.synchronize()
+    check_meta(w, om, gm, status)
+    assert om.status == 0
+
+    qs, qd, ss, sd = m.dispatch_out_shapes(w.mode, w.quant, w.T, w.H, w.K, w.E, w.M)
+    q = torch.empty(qs, dtype=qd, device="cuda")
+    s = torch.empty(ss, dtype=sd, device="cuda") if ss is not None else None
+    st2 = m.new_status()
+    m.moe_dispatch(w.mode, w.quant, x, ids, w.E, gm.src2dst, gm.seg_indptr, q, s, st2, w.M,
+                   w.global_scale or 0.0)
+
+    rows = om.src2dst.astype(np.int64) if w.mode == "normal" else masked_rows(w, om)
+    n = om.num_valid
+    # compact expert outputs, row j belongs to the pair with src2dst == j
+    rng = np.random.default_rng(expert_seed)
+    eo_compact = random_bf16(rng, (n, w.H))
+    pair_of_slot = np.empty(n, np.int64)
+    valid = om.src2dst >= 0
+    pair_of_slot[om.src2dst[valid]] = np.nonzero(valid)[0]
+    if w.mode == "normal":
+        eo = torch.from_numpy(eo_compact.view(np.int16)).cuda().view(torch.bfloat16)
+    else:
+        eo = torch.zeros((w.E * w.M, w.H), dtype=torch.bfloat16, device="cuda")
+        dst = torch.from_numpy(rows[pair_of_slot]).cuda()
+        eo.index_copy_(0, dst, torch.from_numpy(eo_compact.view(np.int16)).cuda().view(torch.bfloat16))
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    st3 = m.new_status()
+    m.moe_combine(w.mode, eo, ids, wt, w.E, gm.src2dst, gm.seg_indptr, out, st3, w.M)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0 and int(st3.item()) == 0
+
+    srng = np.random.default_rng(sample_seed)
+    tokens = np.unique(np.concatenate([[0, w.T - 1], srng.choice(w.T, size=min(n_sample, w.T), replace=False)]))
+    q2 = q.view(-1, q.shape[-1])
+    s2 = s.view(-1, s.shape[-1]) if s is not None else None
+    for t in tokens:
+        t = int(t)
+        if w.quant == "fp8g128":
+            oq, os_ = oracle.quant_fp8_row(w.x[t])
+        elif w.quant == "nvfp4b16":
+            oq, os_ = oracle.quant_nvfp4_row(w.x[t], w.global_scale)
+        else:
+            oq, os_ = w.x[t].view(np.uint8), None
+        for k in range(w.K):
+            r = int(rows[t * w.K + k])
+            if r < 0:
+                continue
+            assert np.array_equal(q2[r].view(torch.uint8).cpu().numpy(), np.ascontiguousarray(oq).view(np.uint8)), (t, k)
+            if os_ is not None:
+                assert np.array_equal(s2[r].view(torch.uint8).cpu().numpy(), np.ascontiguousarray(os_).view(np.uint8)), (t, k)
+    # combine: the oracle on the sampled tokens (normal layout over the compact rows)
+    sub_ids = w.topk_ids[tokens]
+    sub_w = w.topk_weights[tokens]
+    sub_s2d = om.src2dst.reshape(w.T, w.K)[tokens].reshape(-1)
+    sub_meta = oracle.Meta(om.seg_indptr, np.ascontiguousarray(sub_s2d), om.reorder_topk_ids, om.masked_m,
+                           om.partition_counts, om.expected_m, 0)
+    want = oracle.combine("normal", eo_compact, sub_ids, sub_w, sub_meta, w.E)
+    got = out[torch.from_numpy(tokens).cuda()].contiguous()
+    check_combine(bytes_of(got).view(np.uint16).reshape(len(tokens), w.H), want)
+    return om, q, s, out

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Small and medium cases are compared in full (every metadata entry, every output byte
+including the rows the kernels must leave untouched, every combined element); the
+full-size workloads run in the benchmark's launch configuration and are compared in
+full for the metadata and on a seeded sample of tokens for dispatch and combine.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import bf16_bits_to_f32, f32_to_bf16_bits, make_case, make_workload
+
+from _harness import (bytes_of, check_combine, gpu_meta, moe, run_full, run_sampled, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+# --- the named workloads ---------------------------------------------------------
+
+def test_tiny_workload_with_scaled_experts():
+    """tiny: normal / none; expert e returns x * (e+1)/8 (computed on the host, shared)."""
+    m = moe()
+    w = make_workload("tiny")
+    x, ids, wt = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, w.E)
+    gm, st = gpu_meta(w, ids)
+    d = m.dispatch(x, ids, wt, gm, w.E, mode="normal", quant="none", dev_status=st)
+    oq, _ = oracle.dispatch("normal", "none", w.x, w.topk_ids, om, w.E)
+    torch.cuda.synchronize()
+    n = om.num_valid
+    assert np.array_equal(bytes_of(d.hidden_states)[:n], oq[:n].view(np.uint8))
+    rows = bf16_bits_to_f32(oq[:n]).astype(np.float32)
+    scale = ((om.reorder_topk_ids + 1) / 8).astype(np.float32)
+    eo_host = f32_to_bf16_bits(rows * scale[:, None])
+    eo = torch.from_numpy(eo_host.view(np.int16)).cuda().view(torch.bfloat16)
+    y = m.combine(eo, ids, wt, gm, w.E, dev_status=st)
+    want = oracle.combine("normal", eo_host, w.topk_ids, w.topk_weights, om, w.E)
+    torch.cuda.synchronize()
+    check_combine(bytes_of(y).view(np.uint16).reshape(w.T, w.H), want)
+    assert int(st.item()) == 0
+
+
+def test_decode_workload_full():
+    """decode (T=128, H=7168, E=256, top-8, masked M=128, FP8 g128): full comparison."""
+    run_full(make_workload("decode"))
+
+
+@pytest.mark.parametrize("name", ["prefill", "qwen3", "nvfp4"])
+def test_full_size_workloads_sampled(name):
+    run_sampled(make_workload(name))
+
+
+def test_qwen3_masked_secondary():
+    """qwen3 routing in the masked layout with M = T (no capacity drops)."""
+    w = make_workload("qwen3")
+    w.mode, w.M = "masked", w.T
+    run_sampled(w, n_sample=128)
+
+
+# --- shapes: ragged slices, several blocks, limits ------------------------------
+
+@pytest.mark.parametrize("T,H,E,K,mode,quant,M", [
+    (1, 16, 1, 1, "normal", "none", 0),
+    (3, 48, 3, 2, "masked", "none", 4),
+    (37, 272, 5, 3, "normal", "none", 0),          # ragged 512-slice (17 active lanes)
+    (50, 640, 12, 4, "normal", "fp8g128", 0),      # one full + one ragged slice
+    (50, 384, 12, 4, "masked", "fp8g128", 40),
+    (61, 1040, 16, 6, "normal", "nvfp4b16", 0),    # 1040 = 2*512 + 16
+    (61, 208, 16, 6, "masked", "nvfp4b16", 61),
+    (300, 4096, 128, 8, "normal", "none", 0),
+    (200, 7168, 256, 8, "normal", "fp8g128", 0),
+    (200, 7168, 256, 8, "masked", "nvfp4b16", 64),
+    (2500, 256, 37, 8, "normal", "fp8g128", 0),    # 20000 pairs: several route blocks, E not 2^k
+    (3000, 128, 8, 8, "masked", "none", 3000),     # several route blocks with E < 32
+    (1200, 128, 1024, 16, "normal", "none", 0),    # E and K at their limits, several blocks
+    (40, 128, 1024, 16, "masked", "fp8g128", 8),   # E = 1024 in one block
+])
+def test_shapes_full(T, H, E, K, mode, quant, M):
+    w = make_case(T, H, E, K, seed=T + H + E + K, mode=mode, quant=quant, M=M, invalid_rate=0.05)
+    run_full(w)
+
+
+def test_large_route_meta_many_rounds():
+    """2^21 pairs: 16 rounds per warp and 128 blocks; metadata compared in full."""
+    w = make_case(262144, 16, 256, 8, seed=5, routing="zipf")
+    _, ids, _ = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, w.E)
+    gm, st = gpu_meta(w, ids)
+    torch.cuda.synchronize()
+    assert np.array_equal(gm.src2dst.cpu().numpy(), om.src2dst)
+    assert np.array_equal(gm.seg_indptr.cpu().numpy(), om.seg_indptr)
+    assert np.array_equal(gm.reorder_topk_ids[: om.num_valid].cpu().numpy(), om.reorder_topk_ids)
+
+
+# --- degenerate inputs ---------------------------------------------------------------
+
+def test_empty_batch():
+    for mode, quant, M in (("normal", "none", 0), ("masked", "fp8g128", 8), ("masked", "nvfp4b16", 8)):
+        w = make_case(0, 256, 16, 4, mode=mode, quant=quant, M=M)
+        run_full(w)
+
+
+def test_all_slots_invalid():
+    w = make_case(100, 256, 16, 4, seed=3, invalid_rate=1.0)
+    om = run_full(w)
+    assert om.num_valid == 0
+
+
+def test_every_pair_to_one_expert():
+    """All pairs hit expert 0: the warp-match groups are the whole warp."""
+    w = make_case(20000, 128, 4, 1, seed=4, routing="hot", quant="fp8g128")
+    run_full(w)
+
+
+def test_duplicate_experts_in_a_token():
+    w = make_case(500, 256, 6, 8, seed=6, routing="replace", quant="fp8g128")
+    run_full(w)
+
+
+def test_zero_rows_quantise_to_zero_codes():
+    for quant in ("fp8g128", "nvfp4b16"):
+        w = make_case(64, 512, 8, 2, seed=8, quant=quant, zero_tokens=10)
+        run_full(w)
+
+
+def test_capacity_overflow_drops_late_pairs_and_reports():
+    m = moe()
+    w = make_case(400, 256, 4, 2, seed=9, mode="masked", quant="fp8g128", M=100)
+    om = run_full(w)
+    assert om.status == oracle.CAPACITY
+    assert (om.masked_m == 100).any()
+
+
+def test_out_of_range_ids_are_skipped_and_reported():
+    w = make_case(300, 256, 16, 4, seed=10, bad_rate=0.02, invalid_rate=0.02)
+    om = run_full(w)
+    assert om.status == oracle.BAD_ID
+
+
+def test_status_word_is_sticky_first_error_wins():
+    m = moe()
+    w = make_case(64, 256, 8, 2, seed=11, bad_rate=0.1)
+    _, ids, _ = to_dev(w)
+    st = m.new_status()
+    m.route_meta(ids, w.E, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == m.MOE_ERR_BAD_EXPERT_ID
+    w2 = make_case(64, 256, 8, 2, seed=12, mode="masked", M=1)
+    _, ids2, _ = to_dev(w2)
+    m.route_meta(ids2, w2.E, max_tokens_per_expert=1, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == m.MOE_ERR_BAD_EXPERT_ID
+    with pytest.raises(m.MoEError):
+        m.check_status(st)
+
+
+def test_host_errors_raise_before_launch():
+    m = moe()
+    w = make_case(8, 100, 8, 2)
+    x = torch.zeros((8, 100), dtype=torch.bfloat16, device="cuda")
+    _, ids, _ = to_dev(w)
+    gm, st = gpu_meta(w, ids)
+    with pytest.raises(m.MoEError) as e:
+        m.dispatch(x, ids, None, gm, w.E, quant="fp8g128", dev_status=st)
+    assert e.value.status == m.MOE_ERR_INVALID_ARG
+
+
+def test_repeated_calls_reuse_workspace():
+    """The multi-block route workspace is left ready for the next call."""
+    m = moe()
+    w = make_case(5000, 64, 64, 8, seed=13, routing="zipf")
+    _, ids, _ = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, w.E)
+    d = m.MoEDispatcher(w.T, w.H, w.K, w.E)
+    for _ in range(4):
+        d.route(ids)
+        torch.cuda.synchronize()
+        assert np.array_equal(d.src2dst.cpu().numpy(), om.src2dst)
+        assert np.array_equal(d.seg_indptr.cpu().numpy(), om.seg_indptr)
+    d.check()
+
+
+def test_dispatcher_graph_capture_replays_correctly():
+    """route + dispatch + combine captured in one CUDA graph and replayed."""
+    m = moe()
+    w = make_workload("decode")
+    x, ids, wt = to_dev(w)
+    d = m.MoEDispatcher(w.T, w.H, w.K, w.E, mode="masked", quant="fp8g128", num_partitions=w.P,
+                        max_tokens_per_expert=w.M)
+    eo = torch.randn((w.E * w.M, w.H), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        d.route(ids)
+        d.dispatch(x, ids)
+        d.combine(eo, ids, wt)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref_q = d.out_q.clone()
+    ref_out = d.out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        d.route(ids)
+        d.dispatch(x, ids)
+        d.combine(eo, ids, wt)
+    d.out_q.zero_()
+    d.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(d.out_q, ref_q)
+    assert torch.equal(d.out, ref_out)
+    d.check()
