@@ -190,6 +190,8 @@ def test_dispatcher_graph_capture_replays_correctly():
     d = m.MoEDispatcher(w.T, w.H, w.K, w.E, mode="masked", quant="fp8g128", num_partitions=w.P,
                         max_tokens_per_expert=w.M)
     eo = torch.randn((w.E * w.M, w.H), dtype=torch.bfloat16, device="cuda")
+    d.out_q.zero_()            # slots past masked_m are never written: start both runs from zeros
+    d.out.zero_()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
