@@ -58,6 +58,7 @@ _SIGNATURES = {
     "moe_dispatch": (_int, [_int, _int, _P, _i64, _int, _P, _int, _int, _int, _P, _P, _f32, _P, _P, _P, _P]),
     "moe_combine": (_int, [_int, _P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P]),
     "moe_convert_probe": (_int, [_P, _i64, _P, _P, _P, _P]),
+    "moe_route_meta_noalloc": (_int, [_P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 _lib_handle = None
 
@@ -136,6 +137,27 @@ def moe_route_meta(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torch.T
                              _ptr(partition_counts), ctypes.byref(em), _ptr(workspace), ws_bytes,
                              _ptr(dev_status), _stream(stream))
     _check(st, "moe_route_meta")
+    return int(em.value)
+
+
+def moe_route_meta_noalloc(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torch.Tensor,
+                           src2dst: torch.Tensor, reorder_topk_ids: torch.Tensor, masked_m: torch.Tensor,
+                           dev_status: torch.Tensor, num_partitions: int = 1, max_tokens_per_expert: int = 0,
+                           partition_counts: Optional[torch.Tensor] = None, stream=None) -> int:
+    """moe_route_meta for callers that cannot allocate device memory: no workspace argument.
+
+    Scratch comes from a fixed 1 MiB array inside the library (held on every GPU that loads
+    it); larger problems raise MoEError(MOE_ERR_UNSUPPORTED). The first call on a device
+    looks up that array and should come before any stream capture. All calls share the
+    array, so calls that could overlap on the GPU must not be issued. Returns expected_m.
+    """
+    T, K = topk_ids.shape
+    em = ctypes.c_int32(0)
+    st = load_library().moe_route_meta_noalloc(_ptr(topk_ids), T, K, num_experts, num_partitions,
+                                               max_tokens_per_expert, _ptr(seg_indptr), _ptr(src2dst),
+                                               _ptr(reorder_topk_ids), _ptr(masked_m), _ptr(partition_counts),
+                                               ctypes.byref(em), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_route_meta_noalloc")
     return int(em.value)
 
 

@@ -131,6 +131,36 @@ moe_status_t moe_route_meta(const int32_t *topk_ids, int64_t num_tokens, int top
                             int32_t *dev_status, moe_stream_t stream);
 
 /*
+ * moe_route_meta_noalloc -- moe_route_meta without a caller-provided workspace.
+ *
+ * The pages have no counterpart: this is an addition for callers that cannot allocate
+ * device memory at the point they need the metadata -- for example an engine that has
+ * already reserved the GPU's memory for its own pool, a plugin interface that hands over
+ * only input and output pointers, or a path where cudaMalloc's implicit synchronisation
+ * is not acceptable. It computes exactly what moe_route_meta computes, with the same
+ * arguments minus workspace / workspace_bytes, and allocates nothing.
+ *
+ * Scratch: a fixed 1 MiB array in the library's own device memory (every GPU that loads
+ * the library holds it until the process exits). Sizes whose moe_route_meta workspace
+ * would exceed 1 MiB are rejected with MOE_ERR_UNSUPPORTED before anything is launched:
+ * with 1024 experts it covers up to 4,177,920 (token, k) pairs, with 256 experts up to
+ * 16,760,832. Up to 8192 pairs need no scratch at all.
+ * First call on a device: looks up the array's device address with that device current;
+ * make that first call before any stream capture. Each call clears the scratch header
+ * with a cudaMemsetAsync on `stream` before its kernels.
+ * Every call shares the one array, which keeps the previous call's contents: calls whose
+ * kernels may overlap on the GPU (different streams, no ordering between them) race and
+ * must not be issued.
+ * Returns the statuses of moe_route_meta.
+ */
+moe_status_t moe_route_meta_noalloc(const int32_t *topk_ids, int64_t num_tokens, int topk,
+                                    int num_experts, int num_partitions, int max_tokens_per_expert,
+                                    int64_t *seg_indptr, int32_t *src2dst, int32_t *reorder_topk_ids,
+                                    int32_t *masked_m, int32_t *partition_counts,
+                                    int32_t *expected_m_host, int32_t *dev_status,
+                                    moe_stream_t stream);
+
+/*
  * moe_dispatch -- gather (and optionally quantise) token rows into expert order.
  *
  * Operation (the PreReorder permute of _deepep_permute on the diff page; the masked
