@@ -76,6 +76,11 @@ def _load():
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, f32, P, P]),
             "oracle_combine": (None, [ctypes.c_int, P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, P, P, P, P, P]),
+            "oracle_dispatch_layout": (None, [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P]),
+            "oracle_dispatch_partitioned": (None, [ctypes.c_int, P, i64, i64, ctypes.c_int, P, P, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int32, f32, P, P, P, P]),
+            "oracle_combine_partitioned": (None, [P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -232,4 +237,53 @@ def combine(mode: str, expert_out: np.ndarray, topk_ids: np.ndarray, topk_weight
     out = np.empty((T, H), np.uint16)
     _load().oracle_combine(MODES[mode], _ptr(eo), T, H, K, E, M, _ptr(ids), _ptr(meta.src2dst),
                            _ptr(meta.seg_indptr), _ptr(w), _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# per-partition layout (get_dispatch_layout) and the FlashInfer all-to-all layout
+# ---------------------------------------------------------------------------
+
+def dispatch_layout(topk_ids: np.ndarray, E: int, P: int):
+    """(num_tokens_per_rank [P] int32, is_token_in_rank [T, P] bool, num_tokens_per_expert [E] int32)."""
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    T, K = ids.shape
+    ntr = np.zeros(P, np.int32)
+    itr = np.zeros((T, P), np.uint8)
+    nte = np.zeros(E, np.int32)
+    _load().oracle_dispatch_layout(_ptr(ids), T, K, E, P, _ptr(ntr), _ptr(itr), _ptr(nte))
+    return ntr, itr.astype(bool), nte
+
+
+def dispatch_partitioned(quant: str, x: np.ndarray, topk_ids: np.ndarray, topk_weights: np.ndarray, E: int,
+                         P: int, invalid_id: int = -1, global_scale: float = 0.0, num_slots=None, fill: int = 0):
+    """FlashInfer-style receive buffers of one source rank: (recv_x, recv_sf, recv_ids, recv_w)."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    T, H = x.shape
+    K = ids.shape[1]
+    S = T if num_slots is None else num_slots
+    if quant == "nvfp4b16":
+        rx = _filled((P, S, H // 2), np.uint8, fill)
+        rsf = _filled((P, S, H // 16), np.uint8, fill)
+    else:
+        rx = _filled((P, S, H), np.uint16, fill)
+        rsf = None
+    rids = _filled((P, S, K), np.int32, fill)
+    rw = _filled((P, S, K), np.float32, fill)
+    _load().oracle_dispatch_partitioned(QUANTS[quant], _ptr(x), T, S, H, _ptr(ids), _ptr(w), K, E, P,
+                                        int(invalid_id), float(global_scale), _ptr(rx), _ptr(rsf), _ptr(rids),
+                                        _ptr(rw))
+    return rx, rsf, rids, rw
+
+
+def combine_partitioned(partial: np.ndarray, topk_ids: np.ndarray, E: int, P: int) -> np.ndarray:
+    """bf16 bits [T, H]: sum over the partitions each token was sent to of partial[p, t]."""
+    pa = np.ascontiguousarray(partial, dtype=np.uint16)
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    T, K = ids.shape
+    _, S, H = pa.shape
+    out = np.empty((T, H), np.uint16)
+    _load().oracle_combine_partitioned(_ptr(pa), T, S, H, _ptr(ids), K, E, P, _ptr(out))
     return out

@@ -412,3 +412,120 @@ void oracle_combine(int mode, const uint16_t *expert_out, int64_t T, int H, int 
     }
     free(acc);
 }
+
+/* ------------------------------------------------------------------------- */
+/* dispatch layout per expert-parallel partition (get_dispatch_layout)          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * buffer.get_dispatch_layout(topk_ids, num_experts) in
+ * _DeepEPDispatcherImplNormal._dispatch_core ("sglang token_dispatcher/deepep.py" page)
+ * returns num_tokens_per_rank, num_tokens_per_expert and is_token_in_rank (the RDMA-rank
+ * counts belong to the inter-node transport, which has no counterpart here). With P
+ * partitions of E/P experts each:
+ *   is_token_in_rank[t][p]  = 1 iff some valid pair of token t names an expert of p
+ *   num_tokens_per_rank[p]  = #{t : is_token_in_rank[t][p]}
+ *   num_tokens_per_expert[e] = #{valid pairs with id e}
+ */
+void oracle_dispatch_layout(const int32_t *topk_ids, int64_t T, int K, int E, int P,
+                            int32_t *num_tokens_per_rank, uint8_t *is_token_in_rank,
+                            int32_t *num_tokens_per_expert)
+{
+    int ep = E / P;
+    for (int p = 0; p < P; p++) num_tokens_per_rank[p] = 0;
+    if (num_tokens_per_expert)
+        for (int e = 0; e < E; e++) num_tokens_per_expert[e] = 0;
+    for (int64_t t = 0; t < T; t++) {
+        for (int p = 0; p < P; p++) is_token_in_rank[t * P + p] = 0;
+        for (int k = 0; k < K; k++) {
+            int32_t e = topk_ids[t * K + k];
+            if (e < 0 || e >= E) continue;
+            is_token_in_rank[t * P + e / ep] = 1;
+            if (num_tokens_per_expert) num_tokens_per_expert[e]++;
+        }
+        for (int p = 0; p < P; p++) num_tokens_per_rank[p] += is_token_in_rank[t * P + p];
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* FlashInfer all-to-all layout, one source rank (f1)                           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * FlashinferDispatcher.dispatch ("sglang token_dispatcher/flashinfer.py" page): the payload
+ * list [x (or its NVFP4 codes), x_sf, topk_ids, topk_weights] is sent once to every EP rank
+ * that owns at least one of the token's experts, into receive buffers shaped
+ * [ep_size, runtime_max_tokens_per_rank, ...]; the receiver's topk_ids are sanitised so that
+ * experts it does not own, and padding slots, carry invalid_token_expert_id. With one
+ * source rank and P partitions, partition p's receive rows are recv[p][slot] for
+ * slot < num_slots (num_slots = runtime_max_tokens_per_rank >= T). Reading: token t uses
+ * slot t.
+ *   token t routed to p: recv_x[p][t] = Q(x[t]) (quant 0 bf16 copy, 2 NVFP4 codes + sf),
+ *                        recv_ids[p][t][k] = id if id is an expert of p else invalid_id,
+ *                        recv_w[p][t][k] = topk_weights[t][k]
+ *   token not routed to p, and slots t >= T: recv_ids[p][t][k] = invalid_id for all k
+ *                        (the payload and weights of those slots are left untouched).
+ */
+void oracle_dispatch_partitioned(int quant, const uint16_t *x, int64_t T, int64_t num_slots, int H,
+                                 const int32_t *topk_ids, const float *topk_weights, int K, int E, int P,
+                                 int32_t invalid_id, float global_scale, void *recv_x, uint8_t *recv_sf,
+                                 int32_t *recv_ids, float *recv_w)
+{
+    int ep = E / P;
+    size_t row_bytes = quant == 2 ? (size_t)H / 2 : (size_t)H * 2;
+    for (int p = 0; p < P; p++) {
+        for (int64_t t = 0; t < num_slots; t++) {
+            int32_t *ids_out = recv_ids + ((size_t)p * num_slots + t) * K;
+            int routed = 0;
+            if (t < T)
+                for (int k = 0; k < K; k++) {
+                    int32_t e = topk_ids[t * K + k];
+                    if (e >= 0 && e < E && e / ep == p) routed = 1;
+                }
+            if (!routed) {
+                for (int k = 0; k < K; k++) ids_out[k] = invalid_id;
+                continue;
+            }
+            for (int k = 0; k < K; k++) {
+                int32_t e = topk_ids[t * K + k];
+                ids_out[k] = (e >= 0 && e < E && e / ep == p) ? e : invalid_id;
+                recv_w[((size_t)p * num_slots + t) * K + k] = topk_weights[t * K + k];
+            }
+            unsigned char *dst = (unsigned char *)recv_x + ((size_t)p * num_slots + t) * row_bytes;
+            if (quant == 2)
+                oracle_quant_nvfp4_b16_row(x + (size_t)t * H, H, global_scale, dst,
+                                           recv_sf + ((size_t)p * num_slots + t) * (H / 16));
+            else
+                memcpy(dst, x + (size_t)t * H, row_bytes);
+        }
+    }
+}
+
+/*
+ * FlashinferDispatcher.combine (flashinfer.py page): moe_a2a.combine takes each rank's
+ * output [ep_size, runtime_max_tokens_per_rank, H] (already weighted by the MoE runner)
+ * back to the source tokens and sums over the ranks. One source: out[t] = bf16( sum over
+ * the partitions p that received token t, ascending, of partial[p][t] ), binary64
+ * accumulation, one rounding. A token routed nowhere gives zeros.
+ */
+void oracle_combine_partitioned(const uint16_t *partial, int64_t T, int64_t num_slots, int H,
+                                const int32_t *topk_ids, int K, int E, int P, uint16_t *out)
+{
+    int ep = E / P;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)(H > 0 ? H : 1));
+    for (int64_t t = 0; t < T; t++) {
+        for (int h = 0; h < H; h++) acc[h] = 0.0;
+        for (int p = 0; p < P; p++) {
+            int routed = 0;
+            for (int k = 0; k < K; k++) {
+                int32_t e = topk_ids[t * K + k];
+                if (e >= 0 && e < E && e / ep == p) routed = 1;
+            }
+            if (!routed) continue;
+            const uint16_t *src = partial + ((size_t)p * num_slots + t) * H;
+            for (int h = 0; h < H; h++) acc[h] = acc[h] + (double)bf16_to_float(src[h]);
+        }
+        for (int h = 0; h < H; h++) out[(size_t)t * H + h] = oracle_bf16_from_double(acc[h]);
+    }
+    free(acc);
+}
