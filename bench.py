@@ -3,11 +3,12 @@
 combine over one batch of a seeded synthetic workload, on one GB300 per rank.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|qwen3|nvfp4|tiny]
-                    [--impl ours|reference] [--graph]
+                    [--impl ours|reference] [--graph] [--no-fuse]
 
 Prints ONE JSON line (rank 0). ``value`` is whole-job dispatch+combine throughput in tokens/s
 (tokens of all ranks / max-over-ranks mean step time), inputs resident in HBM, L2 flushed
-(256 MiB write) before every step. ``e2e`` repeats the measurement through the public Python
+(256 MiB write + 256 MiB read) before every step; CUDA events around every library call
+give the per-kernel durations. ``--graph`` replays one captured step instead. ``e2e`` repeats the measurement through the public Python
 API with pinned host inputs copied in and the combined output copied out inside the timed
 region. ``roofline`` reports the dominant kernel's algorithmic bytes / CUDA-event duration
 against the measured HBM copy bandwidth. ``cpu_baseline`` times the CPU oracle on a bounded
@@ -259,7 +260,8 @@ def rank_seed(rank: int) -> int:
 def config_of(w) -> dict:
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "K": w.K, "P": w.P, "M": w.M,
             "mode": w.mode, "quant": w.quant, "seed": w.seed, "recipe": w.recipe,
-            "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write)"}
+            "l2": f"flushed before every step ({FLUSH_BYTES >> 20} MiB write, then a {FLUSH_BYTES >> 20} MiB "
+                  f"read so no dirty flush lines remain)"}
 
 
 def run_gpu(args, w, rank, world, dist):
@@ -279,12 +281,26 @@ def run_gpu(args, w, rank, world, dist):
     eo_rows = w.T * w.K if w.mode == "normal" else w.E * w.M
     expert_out = torch.randn((eo_rows, w.H), dtype=torch.bfloat16, device=dev, generator=gen)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_out = torch.empty((), dtype=torch.int32, device=dev)
+
+    def flush_l2(i: int):
+        """Evict L2: write a buffer larger than L2, then read another one, so that the
+        step starts with an L2 full of clean, unrelated lines (no write-back of the
+        flush itself lands inside the timed step)."""
+        flush.fill_(i & 0xff)
+        torch.amax(flush_rd, dim=0, out=flush_out)
     stream = torch.cuda.current_stream()
     route_launches = 1 if moe.moe_route_meta_workspace_size(w.T, w.K, w.E) == 0 else 2
+    # small batches: route + dispatch as one fused kernel (moe_route_dispatch)
+    fused = not args.no_fuse and w.T <= 1024 and w.T * w.K <= 4096
 
     def step():
-        d.route(ids)
-        d.dispatch(x, ids, g)
+        if fused:
+            d.route_dispatch(x, ids, g)
+        else:
+            d.route(ids)
+            d.dispatch(x, ids, g)
         d.combine(expert_out, ids, wt)
 
     # metadata facts for the byte model
@@ -296,41 +312,46 @@ def run_gpu(args, w, rank, world, dist):
     n_rows = int(d.masked_m.sum().item()) if w.mode == "masked" else n_valid
     algo = algorithmic_bytes(w, n_valid, n_rows)
 
+    def timed_step(i, e):
+        flush_l2(i)
+        e[0].record(stream)
+        if graph is not None:
+            graph.replay()
+        elif fused:
+            d.route_dispatch(x, ids, g)
+            e[2].record(stream)
+        else:
+            d.route(ids)
+            e[1].record(stream)
+            d.dispatch(x, ids, g)
+            e[2].record(stream)
+        if graph is None:
+            d.combine(expert_out, ids, wt)
+        e[3].record(stream)
+
     graph = None
     if args.graph:
-        s = torch.cuda.Stream()
-        s.wait_stream(stream)
-        with torch.cuda.stream(s):
+        # one step (the library's launches only) captured once and replayed per step
+        s2 = torch.cuda.Stream()
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
             step()
-        stream.wait_stream(s)
+        stream.wait_stream(s2)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step()
 
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        graph.replay() if graph else step()
+    for i in range(args.warmup):
+        flush_l2(i)
+        graph.replay() if graph is not None else step()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.fill_(i & 0xff)
-        e = ev[i]
-        if graph:
-            e[0].record(stream)
-            graph.replay()
-            e[3].record(stream)
-        else:
-            e[0].record(stream)
-            d.route(ids)
-            e[1].record(stream)
-            d.dispatch(x, ids, g)
-            e[2].record(stream)
-            d.combine(expert_out, ids, wt)
-            e[3].record(stream)
+        timed_step(i, ev[i])
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -342,8 +363,13 @@ def run_gpu(args, w, rank, world, dist):
     value = job_throughput(w.T, world, ms)
 
     kernels = {}
-    if not graph:
-        for name, (a, b) in {"route_meta": (0, 1), "dispatch": (1, 2), "combine": (2, 3)}.items():
+    if graph is None:
+        if fused:
+            algo = {"route_dispatch": algo["route_meta"] + algo["dispatch"], "combine": algo["combine"]}
+            spans = {"route_dispatch": (0, 2), "combine": (2, 3)}
+        else:
+            spans = {"route_meta": (0, 1), "dispatch": (1, 2), "combine": (2, 3)}
+        for name, (a, b) in spans.items():
             us = 1e3 * statistics.mean(e[a].elapsed_time(e[b]) for e in ev)
             kernels[name] = {"us": us, "bytes": algo[name], "gbs": algo[name] / (us * 1e-6) / 1e9}
     peak, peak_kind = measured_hbm_gbs()
@@ -368,19 +394,22 @@ def run_gpu(args, w, rank, world, dist):
             x2.copy_(xp, non_blocking=True)
             ids2.copy_(idp, non_blocking=True)
             wt2.copy_(wtp, non_blocking=True)
-            d.route(ids2)
-            d.dispatch(x2, ids2, g)
+            if fused:
+                d.route_dispatch(x2, ids2, g)
+            else:
+                d.route(ids2)
+                d.dispatch(x2, ids2, g)
             y = d.combine(expert_out, ids2, wt2)
             outp.copy_(y, non_blocking=True)
 
-        for _ in range(max(args.warmup, 1)):
-            flush.fill_(1)
+        for i in range(max(args.warmup, 1)):
+            flush_l2(i)
             e2e_step()
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         torch.cuda.synchronize()
         for i in range(args.steps):
-            flush.fill_(i & 0xff)
+            flush_l2(i)
             ev2[i][0].record(stream)
             e2e_step()
             ev2[i][1].record(stream)
@@ -395,13 +424,15 @@ def run_gpu(args, w, rank, world, dist):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy PCG64 inputs, random expert outputs)",
-        "config": dict(config_of(w), graph=bool(graph), n_valid_pairs=n_valid, rows_moved=n_rows),
+        "config": dict(config_of(w), timing=("CUDA graph of one step, replayed per step" if graph is not None
+                                             else "eager launches, CUDA events around each kernel"),
+                       fused_route_dispatch=fused, n_valid_pairs=n_valid, rows_moved=n_rows),
         "achieved_gbs_step": step_bytes / (ms * 1e-3) / 1e9 / max(world, 1) * world,
         "step_algorithmic_bytes": step_bytes,
         "kernels": kernels,
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": args.steps * (route_launches + 2),
+        "gpu_launches": args.steps * ((1 if fused else route_launches + 1) + 1),
         "clocks": clocks,
     }
     return line
@@ -414,7 +445,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "prefill", "qwen3", "nvfp4"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--graph", action="store_true", help="replay the three launches as one CUDA graph")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step's launches in a CUDA graph and replay it (step time only)")
+    ap.add_argument("--no-fuse", action="store_true", help="separate route_meta and dispatch calls")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

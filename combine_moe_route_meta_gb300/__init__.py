@@ -59,6 +59,12 @@ _SIGNATURES = {
     "moe_combine": (_int, [_int, _P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P]),
     "moe_convert_probe": (_int, [_P, _i64, _P, _P, _P, _P]),
     "moe_route_meta_noalloc": (_int, [_P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_dispatch": (_int, [_int, _int, _P, _i64, _int, _P, _int, _int, _int, _int, _f32, _P, _P, _P, _P,
+                                  _P, _P, _P, _sz, _P, _P, _P, _P]),
+    "moe_dispatch_layout": (_int, [_P, _i64, _int, _int, _int, _P, _P, _P, _P, _P]),
+    "moe_dispatch_partitioned": (_int, [_int, _P, _i64, _i64, _int, _P, _P, _int, _int, _int, _i32, _f32, _P, _P,
+                                        _P, _P, _P, _P]),
+    "moe_combine_partitioned": (_int, [_P, _i64, _i64, _int, _P, _int, _int, _int, _P, _P, _P]),
 }
 _lib_handle = None
 
@@ -110,7 +116,8 @@ def _ptr(t: Optional[torch.Tensor]):
 
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        # the raw handle of torch's current stream, without building a Stream object
+        return ctypes.c_void_p(torch._C._cuda_getCurrentRawStream(torch.cuda.current_device()))
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
@@ -174,6 +181,27 @@ def moe_dispatch(mode: str, quant: str, hidden_states: torch.Tensor, topk_ids: t
     _check(st, "moe_dispatch")
 
 
+def moe_route_dispatch(mode: str, quant: str, hidden_states: torch.Tensor, topk_ids: torch.Tensor,
+                       num_experts: int, seg_indptr: torch.Tensor, src2dst: torch.Tensor,
+                       reorder_topk_ids: torch.Tensor, masked_m: torch.Tensor, out_q: torch.Tensor,
+                       out_scales: Optional[torch.Tensor], dev_status: torch.Tensor,
+                       workspace: Optional[torch.Tensor] = None, num_partitions: int = 1,
+                       max_tokens_per_expert: int = 0, input_global_scale: float = 0.0,
+                       partition_counts: Optional[torch.Tensor] = None, stream=None) -> int:
+    """moe_route_meta + moe_dispatch in one call; returns expected_m."""
+    T, H = hidden_states.shape
+    K = topk_ids.shape[1]
+    em = ctypes.c_int32(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load_library().moe_route_dispatch(
+        MODES[mode], QUANTS[quant], _ptr(hidden_states), T, H, _ptr(topk_ids), K, num_experts, num_partitions,
+        max_tokens_per_expert, float(input_global_scale), _ptr(seg_indptr), _ptr(src2dst), _ptr(reorder_topk_ids),
+        _ptr(masked_m), _ptr(partition_counts), ctypes.byref(em), _ptr(workspace), ws_bytes, _ptr(out_q),
+        _ptr(out_scales), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_route_dispatch")
+    return int(em.value)
+
+
 def moe_combine(mode: str, expert_out: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                 num_experts: int, src2dst: torch.Tensor, seg_indptr: torch.Tensor, out: torch.Tensor,
                 dev_status: torch.Tensor, max_tokens_per_expert: int = 0, stream=None) -> None:
@@ -190,6 +218,40 @@ def moe_convert_probe(x: torch.Tensor, e4m3: Optional[torch.Tensor] = None, e2m1
     """Diagnostics: the quantisers' e4m3 / e2m1 conversions applied to fp32 values ``x``."""
     st = load_library().moe_convert_probe(_ptr(x), x.numel(), _ptr(e4m3), _ptr(e2m1), _ptr(e4m3_value), _stream(stream))
     _check(st, "moe_convert_probe")
+
+
+def moe_dispatch_layout(topk_ids: torch.Tensor, num_experts: int, num_partitions: int,
+                        num_tokens_per_rank: torch.Tensor, is_token_in_rank: torch.Tensor, dev_status: torch.Tensor,
+                        num_tokens_per_expert: Optional[torch.Tensor] = None, stream=None) -> None:
+    T, K = topk_ids.shape
+    st = load_library().moe_dispatch_layout(_ptr(topk_ids), T, K, num_experts, num_partitions,
+                                            _ptr(num_tokens_per_rank), _ptr(is_token_in_rank),
+                                            _ptr(num_tokens_per_expert), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_dispatch_layout")
+
+
+def moe_dispatch_partitioned(quant: str, hidden_states: torch.Tensor, topk_ids: torch.Tensor,
+                             topk_weights: torch.Tensor, num_experts: int, num_partitions: int,
+                             recv_x: torch.Tensor, recv_scales: Optional[torch.Tensor], recv_topk_ids: torch.Tensor,
+                             recv_topk_weights: torch.Tensor, dev_status: torch.Tensor, invalid_expert_id: int = -1,
+                             input_global_scale: float = 0.0, stream=None) -> None:
+    T, H = hidden_states.shape
+    K = topk_ids.shape[1]
+    S = recv_topk_ids.shape[1]
+    st = load_library().moe_dispatch_partitioned(
+        QUANTS[quant], _ptr(hidden_states), T, S, H, _ptr(topk_ids), _ptr(topk_weights), K, num_experts,
+        num_partitions, int(invalid_expert_id), float(input_global_scale), _ptr(recv_x), _ptr(recv_scales),
+        _ptr(recv_topk_ids), _ptr(recv_topk_weights), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_dispatch_partitioned")
+
+
+def moe_combine_partitioned(partial: torch.Tensor, topk_ids: torch.Tensor, num_experts: int, num_partitions: int,
+                            out: torch.Tensor, dev_status: torch.Tensor, stream=None) -> None:
+    T, K = topk_ids.shape
+    _, S, H = partial.shape
+    st = load_library().moe_combine_partitioned(_ptr(partial), T, S, H, _ptr(topk_ids), K, num_experts,
+                                                num_partitions, _ptr(out), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_combine_partitioned")
 
 
 # ---------------------------------------------------------------------------
@@ -340,6 +402,15 @@ class MoEDispatcher:
         self.expected_m = moe_route_meta(topk_ids, self.E, self.seg_indptr, self.src2dst, self.reorder_topk_ids,
                                          self.masked_m, self.status, self.workspace, self.P, self.M,
                                          self.partition_counts, stream)
+        return self.expected_m
+
+    def route_dispatch(self, hidden_states: torch.Tensor, topk_ids: torch.Tensor, input_global_scale: float = 0.0,
+                       stream=None) -> int:
+        """route() and dispatch() in one library call (one kernel for small batches)."""
+        self.expected_m = moe_route_dispatch(self.mode, self.quant, hidden_states, topk_ids, self.E, self.seg_indptr,
+                                             self.src2dst, self.reorder_topk_ids, self.masked_m, self.out_q,
+                                             self.out_scales, self.status, self.workspace, self.P, self.M,
+                                             input_global_scale, self.partition_counts, stream)
         return self.expected_m
 
     def dispatch(self, hidden_states: torch.Tensor, topk_ids: torch.Tensor, input_global_scale: float = 0.0,

@@ -8,10 +8,12 @@
 //
 // Design: HBM-bound K-way gather. One warp per (token, 512-column slice); each lane owns
 // 16 columns. Lanes 0..K-1 fetch the slot metadata (row, weight) and broadcast it by
-// shuffle; each lane then issues the loads of up to 8 source rows (2 x 16 B per row,
-// ld.global.nc with L1::no_allocate) before consuming any, so a warp keeps 8 KB in
-// flight. Accumulation order is fixed (k ascending) and the result is rounded once to
-// bf16 (cvt.rn.bf16x2). A token with no valid slot gets zeros.
+// shuffle (the masked layout reads seg_indptr from a shared-memory copy). Each lane then
+// issues the loads of up to 8 source rows (2 x 16 B per row, ld.global.nc with
+// L1::no_allocate) before consuming any, so a warp keeps 8 KB in flight, and the next
+// unit's slot metadata is fetched alongside. Accumulation order is fixed (k ascending)
+// and the result is rounded once to bf16 (cvt.rn.bf16x2). A token with no valid slot
+// gets zeros. Small grids use smaller blocks so that every SM gets a similar share.
 #include <cstdint>
 
 #include "moe_device.cuh"
@@ -40,41 +42,65 @@ struct CombineArgs {
     int64_t max_row;
 };
 
+// Slot metadata of pair t*K + lane as loaded from memory (lanes >= K hold d = -1).
+struct SlotMeta {
+    int d;    // src2dst
+    int e;    // expert id (masked layout only)
+    float w;  // topk weight
+};
+
+template <bool MASKED>
+__device__ __forceinline__ SlotMeta load_slot(const CombineArgs& a, int64_t t, int lane) {
+    SlotMeta m{-1, -1, 0.0f};
+    if (lane < a.K) {
+        const int64_t i = t * a.K + lane;
+        m.d = __ldg(a.src2dst + i);
+        m.w = __ldg(a.w + i);
+        if (MASKED) m.e = __ldg(a.ids + i);
+    }
+    return m;
+}
+
+template <bool MASKED>
+__device__ __forceinline__ int64_t slot_row(const CombineArgs& a, const int* s_seg, const SlotMeta& m) {
+    if (m.d < 0) return -1;
+    if (MASKED) {
+        if (m.e < 0 || m.e >= a.E) {
+            set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
+            return -1;
+        }
+        const int rank = m.d - s_seg[m.e];
+        return (rank >= 0 && rank < a.M) ? int64_t(m.e) * a.M + rank : -1;
+    }
+    if (m.d < a.max_row) return m.d;
+    set_status(a.status, MOE_ERR_INVALID_ARG);
+    return -1;
+}
+
 template <bool MASKED>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
+    extern __shared__ int s_seg[];  // [E] in masked mode
+    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int H = a.H;
 
-    for (int64_t u = warp; u < a.n_units; u += nwarps) {
+    // the first unit's slot metadata is in flight while seg_indptr is staged
+    int64_t u = warp;
+    SlotMeta meta = load_slot<MASKED>(a, u < a.n_units ? u / a.units_per_row : 0, u < a.n_units ? lane : 32);
+    if (MASKED) {
+        for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_seg[e] = int(a.seg[e]);
+        __syncthreads();
+    }
+
+    for (; u < a.n_units; u += nwarps) {
         const int64_t t = u / a.units_per_row;
         const int col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
         const bool active = col < H;
-
-        int64_t my_row = -1;
-        float my_w = 0.0f;
-        if (lane < a.K) {
-            const int64_t i = t * a.K + lane;
-            const int d = __ldg(a.src2dst + i);
-            my_w = __ldg(a.w + i);
-            if (d >= 0) {
-                if (MASKED) {
-                    const int e = __ldg(a.ids + i);
-                    if (e >= 0 && e < a.E) {
-                        const int64_t rank = int64_t(d) - __ldg(a.seg + e);
-                        if (rank >= 0 && rank < a.M) my_row = int64_t(e) * a.M + rank;
-                    } else {
-                        set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
-                    }
-                } else if (d < a.max_row) {
-                    my_row = d;
-                } else {
-                    set_status(a.status, MOE_ERR_INVALID_ARG);
-                }
-            }
-        }
+        const int64_t my_row = slot_row<MASKED>(a, s_seg, meta);
+        const float my_w = meta.w;
 
         float acc[kLaneElems];
 #pragma unroll
@@ -102,6 +128,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
                     v[j][1] = v[j][0];
                 }
             }
+            // the next unit's slot metadata rides along with this unit's row loads
+            if (k0 + kBatch >= a.K) {
+                const int64_t un = u + nwarps;
+                meta = load_slot<MASKED>(a, un < a.n_units ? un / a.units_per_row : 0, un < a.n_units ? lane : 32);
+            }
 #pragma unroll
             for (int j = 0; j < kBatch; j++) {
                 if (rows[j] >= 0) {
@@ -126,26 +157,18 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
 template <bool MASKED>
 cudaError_t launch_variant(const LaunchCtx& ctx, const CombineArgs& a) {
     auto kern = combine_kernel<MASKED>;
+    const size_t smem = MASKED ? sizeof(int) * size_t(a.E) : 0;
+    // one wave or less of 256-thread blocks leaves SMs unevenly loaded: use 64 threads
+    const int threads = a.n_units < int64_t(ctx.num_sms) * 16 ? 64 : kCombineThreads;
     int per_sm = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCombineThreads, 0);
+    cudaError_t err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
     if (err != cudaSuccess) return err;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t warps_per_block = kCombineThreads / 32;
+    const int64_t warps_per_block = threads / 32;
     const int64_t need = (a.n_units + warps_per_block - 1) / warps_per_block;
     const int64_t cap = int64_t(ctx.num_sms) * per_sm;
     const int grid = int(need < cap ? need : cap);
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a);
 }
 
 }  // namespace

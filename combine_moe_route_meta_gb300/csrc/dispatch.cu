@@ -16,22 +16,20 @@
 //
 // Design: HBM-bound gather; the read of each token row happens once and the K
 // destination rows are written from registers.
-//  * Work unit = (token t, a 512-element column slice). One warp per unit; each lane
-//    owns 16 consecutive elements (two 16-byte loads with L1::no_allocate).
+//  * Work unit = (token t, a 512-element column slice). One warp per unit; each lane owns
+//    16 consecutive elements (two 16-byte loads with L1::no_allocate).
 //  * The K destination rows of the token are resolved by lanes 0..K-1 and broadcast
-//    with shuffles while the row loads are in flight.
+//    with shuffles while the row loads are in flight. In the masked layout the block
+//    first stages seg_indptr in shared memory, so a slot index costs no dependent load.
 //  * FP8: a 128-element group spans 8 lanes; its amax is a 3-step xor-shuffle. NVFP4:
-//    a 16-element block is one lane, so its amax needs no shuffle.
-//  * Every division and multiplication of the quantiser is an explicit
-//    round-to-nearest binary32 operation (__fdiv_rn / __fmul_rn), and the conversions
-//    are the hardware cvt.rn.satfinite instructions, so the codes are a deterministic
-//    function of the input bits.
+//    a 16-element block is one lane, so its amax needs no shuffle (dispatch_slice.cuh).
 //  * Stores are 16-byte (bf16, e4m3) or 8-byte (e2m1) vectors; a warp writes a
 //    contiguous 1 KB / 512 B / 256 B span of each destination row.
 //  * Grid-stride over units with a grid of (SMs x resident blocks); the warp-to-unit
 //    order walks a token's slices with neighbouring warps.
 #include <cstdint>
 
+#include "dispatch_slice.cuh"
 #include "moe_device.cuh"
 #include "moe_launch.h"
 
@@ -58,9 +56,9 @@ struct DispatchArgs {
     int64_t max_row;  // exclusive bound on normal-mode rows (T*K)
 };
 
-// destination row of pair t*K + lane (lanes >= K return -1)
+// destination row of pair t*K + lane (lanes >= K return -1); s_seg: seg_indptr in smem
 template <bool MASKED>
-__device__ __forceinline__ int64_t dest_row(const DispatchArgs& a, int64_t t, int lane) {
+__device__ __forceinline__ int64_t dest_row(const DispatchArgs& a, const int* s_seg, int64_t t, int lane) {
     int64_t row = -1;
     if (lane < a.K) {
         const int64_t i = t * a.K + lane;
@@ -69,7 +67,7 @@ __device__ __forceinline__ int64_t dest_row(const DispatchArgs& a, int64_t t, in
             if (MASKED) {
                 const int e = __ldg(a.ids + i);
                 if (e >= 0 && e < a.E) {
-                    const int64_t rank = int64_t(d) - __ldg(a.seg + e);
+                    const int rank = d - s_seg[e];
                     if (rank >= 0 && rank < a.M) row = int64_t(e) * a.M + rank;
                 } else {
                     set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
@@ -86,119 +84,53 @@ __device__ __forceinline__ int64_t dest_row(const DispatchArgs& a, int64_t t, in
 
 template <int QUANT, bool MASKED>
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs a) {
+    extern __shared__ int s_seg[];  // [E] in masked mode
+    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
     const int H = a.H;
 
-    for (int64_t u = warp; u < a.n_units; u += nwarps) {
-        const int64_t t = u / a.units_per_row;
-        const int col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
-        const bool active = col < H;
-        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-        if (active) {
-            const uint16_t* src = a.x + t * H + col;
-            v0 = ld_stream_v4(src);
-            v1 = ld_stream_v4(src + 8);
-        }
-        const int64_t my_row = dest_row<MASKED>(a, t, lane);
+    // the first unit's row slice is in flight while seg_indptr is staged
+    int64_t u = warp;
+    int64_t t = u < a.n_units ? u / a.units_per_row : 0;
+    int col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
+    bool active = u < a.n_units && col < H;
+    LaneSlice sl{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (active) sl = load_slice(a.x + t * H + col);
+    if (MASKED) {
+        for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_seg[e] = int(a.seg[e]);
+        __syncthreads();
+    }
 
-        if constexpr (QUANT == MOE_QUANT_NONE) {
-            uint16_t* out = static_cast<uint16_t*>(a.out_q);
-            for (int k = 0; k < a.K; k++) {
-                const int64_t row = __shfl_sync(kFullMask, my_row, k);
-                if (row >= 0 && active) {
-                    uint16_t* dst = out + row * H + col;
-                    st_v4(dst, v0);
-                    st_v4(dst + 8, v1);
-                }
-            }
-        } else if constexpr (QUANT == MOE_QUANT_FP8_G128) {
-            float f[16];
-            unpack8(v0, f);
-            unpack8(v1, f + 8);
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
-            // a 128-element group is 8 aligned lanes
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-            const float s = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-            uint32_t w[4];
-#pragma unroll
-            for (int p = 0; p < 4; p++) {
-                const uint32_t lo = e4m3x2(__fdiv_rn(f[4 * p], s), __fdiv_rn(f[4 * p + 1], s));
-                const uint32_t hi = e4m3x2(__fdiv_rn(f[4 * p + 2], s), __fdiv_rn(f[4 * p + 3], s));
-                w[p] = lo | (hi << 16);
-            }
-            const uint4 q = make_uint4(w[0], w[1], w[2], w[3]);
-            uint8_t* out = static_cast<uint8_t*>(a.out_q);
-            float* scales = static_cast<float*>(a.out_s);
-            const int groups = H / 128;
-            for (int k = 0; k < a.K; k++) {
-                const int64_t row = __shfl_sync(kFullMask, my_row, k);
-                if (row >= 0 && active) {
-                    st_v4(out + row * H + col, q);
-                    if ((lane & 7) == 0) scales[row * groups + col / 128] = s;
-                }
-            }
-        } else {  // MOE_QUANT_NVFP4_B16
-            float f[16];
-            unpack8(v0, f);
-            unpack8(v1, f + 8);
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
-            const float tsf = __fmul_rn(__fdiv_rn(amax, 6.0f), a.g);
-            const uint32_t sf = e4m3x2(tsf, 0.0f) & 0xffu;
-            const float sff = e4m3_value(sf);
-            uint2 q = make_uint2(0, 0);
-            if (sff != 0.0f) {
-                const float r = __fdiv_rn(a.g, sff);
-                uint32_t b[8];
-#pragma unroll
-                for (int p = 0; p < 8; p++) b[p] = e2m1x2(__fmul_rn(f[2 * p], r), __fmul_rn(f[2 * p + 1], r));
-                q.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-                q.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-            }
-            uint8_t* out = static_cast<uint8_t*>(a.out_q);
-            uint8_t* sfo = static_cast<uint8_t*>(a.out_s);
-            for (int k = 0; k < a.K; k++) {
-                const int64_t row = __shfl_sync(kFullMask, my_row, k);
-                if (row >= 0 && active) {
-                    st_v2(out + row * (H / 2) + col / 2, q);
-                    sfo[row * (H / 16) + col / 16] = uint8_t(sf);
-                }
-            }
-        }
+    while (u < a.n_units) {
+        const int64_t my_row = dest_row<MASKED>(a, s_seg, t, lane);
+        quantise_store<QUANT>(sl, active, lane, col, H, a.K, my_row, a.g, a.out_q, a.out_s);
+        u += nwarps;
+        if (u >= a.n_units) break;
+        t = u / a.units_per_row;
+        col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
+        active = col < H;
+        if (active) sl = load_slice(a.x + t * H + col);
     }
 }
 
 template <int QUANT, bool MASKED>
 cudaError_t launch_variant(const LaunchCtx& ctx, const DispatchArgs& a) {
     auto kern = dispatch_kernel<QUANT, MASKED>;
+    const size_t smem = MASKED ? sizeof(int) * size_t(a.E) : 0;
+    // one wave or less of 256-thread blocks leaves SMs unevenly loaded: use 64 threads
+    const int threads = a.n_units < int64_t(ctx.num_sms) * 16 ? 64 : kDispatchThreads;
     int per_sm = 0;
-    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDispatchThreads, 0);
+    cudaError_t err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
     if (err != cudaSuccess) return err;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t warps_per_block = kDispatchThreads / 32;
+    const int64_t warps_per_block = threads / 32;
     const int64_t need = (a.n_units + warps_per_block - 1) / warps_per_block;
     const int64_t cap = int64_t(ctx.num_sms) * per_sm;
     const int grid = int(need < cap ? need : cap);
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kDispatchThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a);
 }
 
 __global__ void convert_probe_kernel(const float* __restrict__ in, int64_t n_pairs, uint8_t* e4m3,

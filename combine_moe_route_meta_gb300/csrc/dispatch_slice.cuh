@@ -1,0 +1,110 @@
+// dispatch_slice.cuh -- quantise one lane's 16 elements of a token row and store them into
+// the K destination rows (shared by the dispatch kernels).
+//
+// Q = identity, FP8 e4m3 per 128-element group (sglang_per_token_group_quant_fp8 in
+// _DeepEPDispatcherImplNormal.dispatch_a, "sglang token_dispatcher/deepep.py" page), or
+// NVFP4 e2m1 with an e4m3 scale per 16-element block (fp4_quantize in
+// FlashinferDispatcher.dispatch, "sglang token_dispatcher/flashinfer.py" page):
+//   fp8:   s = max(amax, 1e-10) / 448,           q = e4m3(x / s)
+//   nvfp4: sf = e4m3((amax / 6) * g),             q = e2m1(x * (g / value(sf))), 0 if sf == 0
+// Every division and multiplication is an explicit round-to-nearest binary32 operation
+// (__fdiv_rn / __fmul_rn) and the conversions are cvt.rn.satfinite, so the codes are a
+// deterministic function of the input bits.
+#pragma once
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+// One lane's payload: 16 bf16 elements (two 16-byte vectors) of a token row.
+struct LaneSlice {
+    uint4 v0, v1;
+};
+
+__device__ __forceinline__ LaneSlice load_slice(const uint16_t* src) {
+    LaneSlice s;
+    s.v0 = ld_stream_v4(src);
+    s.v1 = ld_stream_v4(src + 8);
+    return s;
+}
+
+// Quantise `s` (the lane's 16 elements starting at column `col`, lane index `lane`) and
+// write it to every destination row: row k of the token is __shfl(my_row, k), -1 = none.
+// All 32 lanes of the warp must call this together (the FP8 group amax and the row
+// broadcast are warp shuffles); `active` is false for lanes past the end of the row.
+template <int QUANT>
+__device__ __forceinline__ void quantise_store(const LaneSlice& s, bool active, int lane, int col, int H,
+                                               int K, int64_t my_row, float g, void* out_q,
+                                               void* out_s) {
+    if constexpr (QUANT == MOE_QUANT_NONE) {
+        uint16_t* out = static_cast<uint16_t*>(out_q);
+        for (int k = 0; k < K; k++) {
+            const int64_t row = __shfl_sync(kFullMask, my_row, k);
+            if (row >= 0 && active) {
+                uint16_t* dst = out + row * H + col;
+                st_v4(dst, s.v0);
+                st_v4(dst + 8, s.v1);
+            }
+        }
+    } else if constexpr (QUANT == MOE_QUANT_FP8_G128) {
+        float f[16];
+        unpack8(s.v0, f);
+        unpack8(s.v1, f + 8);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
+        // a 128-element group is 8 aligned lanes
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+        const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            const uint32_t lo = e4m3x2(__fdiv_rn(f[4 * p], sc), __fdiv_rn(f[4 * p + 1], sc));
+            const uint32_t hi = e4m3x2(__fdiv_rn(f[4 * p + 2], sc), __fdiv_rn(f[4 * p + 3], sc));
+            w[p] = lo | (hi << 16);
+        }
+        const uint4 q = make_uint4(w[0], w[1], w[2], w[3]);
+        uint8_t* out = static_cast<uint8_t*>(out_q);
+        float* scales = static_cast<float*>(out_s);
+        const int groups = H / 128;
+        for (int k = 0; k < K; k++) {
+            const int64_t row = __shfl_sync(kFullMask, my_row, k);
+            if (row >= 0 && active) {
+                st_v4(out + row * H + col, q);
+                if ((lane & 7) == 0) scales[row * groups + col / 128] = sc;
+            }
+        }
+    } else {  // MOE_QUANT_NVFP4_B16
+        float f[16];
+        unpack8(s.v0, f);
+        unpack8(s.v1, f + 8);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
+        const float tsf = __fmul_rn(__fdiv_rn(amax, 6.0f), g);
+        const uint32_t sf = e4m3x2(tsf, 0.0f) & 0xffu;
+        const float sff = e4m3_value(sf);
+        uint2 q = make_uint2(0, 0);
+        if (sff != 0.0f) {
+            const float r = __fdiv_rn(g, sff);
+            uint32_t b[8];
+#pragma unroll
+            for (int p = 0; p < 8; p++) b[p] = e2m1x2(__fmul_rn(f[2 * p], r), __fmul_rn(f[2 * p + 1], r));
+            q.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+            q.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+        }
+        uint8_t* out = static_cast<uint8_t*>(out_q);
+        uint8_t* sfo = static_cast<uint8_t*>(out_s);
+        for (int k = 0; k < K; k++) {
+            const int64_t row = __shfl_sync(kFullMask, my_row, k);
+            if (row >= 0 && active) {
+                st_v2(out + row * (H / 2) + col / 2, q);
+                sfo[row * (H / 16) + col / 16] = uint8_t(sf);
+            }
+        }
+    }
+}
+
+}  // namespace moe

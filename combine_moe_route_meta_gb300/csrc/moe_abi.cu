@@ -21,6 +21,7 @@ moe_status_t make_ctx(moe_stream_t stream, moe::LaunchCtx* ctx) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
     ctx->stream = reinterpret_cast<cudaStream_t>(stream);
     ctx->num_sms = sms > 0 ? sms : 1;
+    ctx->device = dev;
     return MOE_OK;
 }
 
@@ -120,6 +121,57 @@ moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t* hi
                                           input_global_scale, out_q, out_scales, dev_status));
 }
 
+moe_status_t moe_route_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t* hidden_states,
+                                int64_t num_tokens, int hidden, const int32_t* topk_ids, int topk,
+                                int num_experts, int num_partitions, int max_tokens_per_expert,
+                                float input_global_scale, int64_t* seg_indptr, int32_t* src2dst,
+                                int32_t* reorder_topk_ids, int32_t* masked_m, int32_t* partition_counts,
+                                int32_t* expected_m_host, void* workspace, size_t workspace_bytes,
+                                void* out_q, void* out_scales, int32_t* dev_status, moe_stream_t stream) {
+    if (mode != MOE_MODE_NORMAL && mode != MOE_MODE_MASKED) return MOE_ERR_INVALID_ARG;
+    if (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_G128 && quant != MOE_QUANT_NVFP4_B16)
+        return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_shape(num_tokens, topk, num_experts);
+    if (st != MOE_OK) return st;
+    if (num_partitions < 1 || num_experts % num_partitions != 0) return MOE_ERR_INVALID_ARG;
+    if (hidden <= 0 || hidden % 16 != 0) return MOE_ERR_INVALID_ARG;
+    if (quant == MOE_QUANT_FP8_G128 && hidden % 128 != 0) return MOE_ERR_INVALID_ARG;
+    const bool masked = mode == MOE_MODE_MASKED;
+    if (masked ? max_tokens_per_expert < 1 : max_tokens_per_expert < 0) return MOE_ERR_INVALID_ARG;
+    if (!seg_indptr || !masked_m || !dev_status) return MOE_ERR_INVALID_ARG;
+    const int64_t n_pairs = num_tokens * topk;
+    if (n_pairs > 0 && (!topk_ids || !src2dst || !reorder_topk_ids || !hidden_states || !out_q))
+        return MOE_ERR_INVALID_ARG;
+    if (n_pairs > 0 && quant != MOE_QUANT_NONE && !out_scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(seg_indptr, 8) || !aligned(topk_ids, 4) || !aligned(src2dst, 4) ||
+        !aligned(reorder_topk_ids, 4) || !aligned(masked_m, 4) || !aligned(partition_counts, 4) ||
+        !aligned(dev_status, 4) || !aligned(hidden_states, 16) || !aligned(out_q, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (quant == MOE_QUANT_FP8_G128 && !aligned(out_scales, 4)) return MOE_ERR_INVALID_ARG;
+    const int M = masked ? max_tokens_per_expert : 0;
+    const bool fused = moe::route_dispatch_fusable(num_tokens, topk);
+    const moe::RoutePlan plan = moe::plan_route_meta(n_pairs, num_experts);
+    if (!fused && plan.ws_bytes > 0 &&
+        (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)))
+        return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    if (expected_m_host) *expected_m_host = int32_t((n_pairs + num_experts) / num_experts);
+    if (fused)
+        return from_cuda(moe::launch_route_dispatch_small(
+            ctx, int(mode), int(quant), hidden_states, num_tokens, hidden, topk_ids, topk, num_experts,
+            num_partitions, M, input_global_scale, seg_indptr, src2dst, reorder_topk_ids, masked_m,
+            partition_counts, out_q, out_scales, dev_status));
+    st = from_cuda(moe::launch_route_meta(ctx, plan, topk_ids, n_pairs, topk, num_experts, num_partitions,
+                                          M, seg_indptr, src2dst, reorder_topk_ids, masked_m,
+                                          partition_counts, workspace, dev_status));
+    if (st != MOE_OK || num_tokens == 0) return st;
+    return from_cuda(moe::launch_dispatch(ctx, int(mode), int(quant), hidden_states, num_tokens, hidden,
+                                          topk_ids, topk, num_experts, M, src2dst, seg_indptr,
+                                          input_global_scale, out_q, out_scales, dev_status));
+}
+
 moe_status_t moe_combine(moe_mode_t mode, const uint16_t* expert_out, int64_t num_tokens, int hidden,
                          int topk, int num_experts, int max_tokens_per_expert,
                          const int32_t* topk_ids, const int32_t* src2dst, const int64_t* seg_indptr,
@@ -145,6 +197,78 @@ moe_status_t moe_combine(moe_mode_t mode, const uint16_t* expert_out, int64_t nu
     return from_cuda(moe::launch_combine(ctx, int(mode), expert_out, num_tokens, hidden, topk,
                                          num_experts, masked ? max_tokens_per_expert : 0, topk_ids,
                                          src2dst, seg_indptr, topk_weights, out, dev_status));
+}
+
+moe_status_t moe_dispatch_layout(const int32_t* topk_ids, int64_t num_tokens, int topk, int num_experts,
+                                 int num_partitions, int32_t* num_tokens_per_rank, uint8_t* is_token_in_rank,
+                                 int32_t* num_tokens_per_expert, int32_t* dev_status, moe_stream_t stream) {
+    moe_status_t st = check_shape(num_tokens, topk, num_experts);
+    if (st != MOE_OK) return st;
+    if (num_partitions < 1 || num_experts % num_partitions != 0) return MOE_ERR_INVALID_ARG;
+    if (!num_tokens_per_rank || !dev_status) return MOE_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!topk_ids || !is_token_in_rank)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_ids, 4) || !aligned(num_tokens_per_rank, 4) || !aligned(num_tokens_per_expert, 4) ||
+        !aligned(dev_status, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_dispatch_layout(ctx, topk_ids, num_tokens, topk, num_experts, num_partitions,
+                                                 num_tokens_per_rank, is_token_in_rank, num_tokens_per_expert,
+                                                 dev_status));
+}
+
+static moe_status_t check_partitioned(int64_t T, int64_t S, int H, int K, int E, int P) {
+    moe_status_t st = check_shape(T, K, E);
+    if (st != MOE_OK) return st;
+    if (P < 1 || E % P != 0 || S < T) return MOE_ERR_INVALID_ARG;
+    if (P > moe::kMaxPartitionsA2A) return MOE_ERR_UNSUPPORTED;
+    if (S > 0 && S * P > int64_t(INT32_MAX) / (K > 0 ? K : 1)) return MOE_ERR_UNSUPPORTED;
+    if (H <= 0 || H % 16 != 0) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t* hidden_states, int64_t num_tokens,
+                                      int64_t num_slots, int hidden, const int32_t* topk_ids,
+                                      const float* topk_weights, int topk, int num_experts, int num_partitions,
+                                      int32_t invalid_expert_id, float input_global_scale, void* recv_x,
+                                      uint8_t* recv_scales, int32_t* recv_topk_ids, float* recv_topk_weights,
+                                      int32_t* dev_status, moe_stream_t stream) {
+    if (quant != MOE_QUANT_NONE && quant != MOE_QUANT_NVFP4_B16) return MOE_ERR_INVALID_ARG;
+    moe_status_t st = check_partitioned(num_tokens, num_slots, hidden, topk, num_experts, num_partitions);
+    if (st != MOE_OK) return st;
+    if (!dev_status) return MOE_ERR_INVALID_ARG;
+    if (num_slots == 0) return MOE_OK;
+    if (!recv_topk_ids || !recv_topk_weights || !recv_x) return MOE_ERR_INVALID_ARG;
+    if (num_tokens > 0 && (!hidden_states || !topk_ids || !topk_weights)) return MOE_ERR_INVALID_ARG;
+    if (quant == MOE_QUANT_NVFP4_B16 && !recv_scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned(hidden_states, 16) || !aligned(recv_x, 16) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
+        !aligned(recv_topk_ids, 4) || !aligned(recv_topk_weights, 4) || !aligned(dev_status, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_dispatch_partitioned(ctx, int(quant), hidden_states, num_tokens, num_slots, hidden,
+                                                      topk_ids, topk_weights, topk, num_experts, num_partitions,
+                                                      invalid_expert_id, input_global_scale, recv_x, recv_scales,
+                                                      recv_topk_ids, recv_topk_weights, dev_status));
+}
+
+moe_status_t moe_combine_partitioned(const uint16_t* partial, int64_t num_tokens, int64_t num_slots, int hidden,
+                                     const int32_t* topk_ids, int topk, int num_experts, int num_partitions,
+                                     uint16_t* out, int32_t* dev_status, moe_stream_t stream) {
+    moe_status_t st = check_partitioned(num_tokens, num_slots, hidden, topk, num_experts, num_partitions);
+    if (st != MOE_OK) return st;
+    if (!dev_status) return MOE_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MOE_OK;
+    if (!partial || !topk_ids || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(partial, 16) || !aligned(out, 16) || !aligned(topk_ids, 4) || !aligned(dev_status, 4))
+        return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_combine_partitioned(ctx, partial, num_tokens, num_slots, hidden, topk_ids, topk,
+                                                     num_experts, num_partitions, out, dev_status));
 }
 
 moe_status_t moe_convert_probe(const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1,

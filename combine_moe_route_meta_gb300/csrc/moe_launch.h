@@ -2,8 +2,11 @@
 // Arguments arrive here already validated by moe_abi.cu.
 #pragma once
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 namespace moe {
@@ -12,7 +15,64 @@ namespace moe {
 struct LaunchCtx {
     cudaStream_t stream;
     int num_sms;
+    int device;
 };
+
+// Launch `kern` as a programmatic dependent of the previous kernel in the stream: its
+// launch may overlap that kernel's execution, and every kernel of this library executes
+// griddepcontrol.wait before its first global-memory access, so it still sees all of the
+// previous kernel's writes.
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(const LaunchCtx& ctx, Kernel kern, dim3 grid, dim3 block, size_t smem, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Resident blocks per SM of `kern` at (threads, smem), cached per device: the answer
+// depends only on the compiled kernel and the device, so it is queried once.
+template <typename Kernel>
+cudaError_t blocks_per_sm(const LaunchCtx& ctx, Kernel kern, int threads, size_t smem, int* out) {
+    constexpr int kDevices = 64, kSlots = 4;
+    struct Entry {
+        int threads;
+        size_t smem;
+        int value;
+    };
+    static std::mutex mu;
+    static Entry cache[kDevices][kSlots] = {};
+    const int dev = ctx.device >= 0 && ctx.device < kDevices ? ctx.device : -1;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        for (const Entry& e : cache[dev])
+            if (e.value > 0 && e.threads == threads && e.smem == smem) {
+                *out = e.value;
+                return cudaSuccess;
+            }
+    }
+    int v = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, smem);
+    if (err != cudaSuccess) return err;
+    if (v < 1) v = 1;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        for (Entry& e : cache[dev])
+            if (e.value == 0) {
+                e = Entry{threads, smem, v};
+                break;
+            }
+    }
+    *out = v;
+    return cudaSuccess;
+}
 
 // Route metadata: pairs are cut into chunks of 1024*R consecutive pairs, one per
 // thread block. One block handles everything when n_pairs <= kRouteSingleMax.
@@ -38,6 +98,29 @@ cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uin
                             int H, const int32_t* topk_ids, int K, int E, int M,
                             const int32_t* src2dst, const int64_t* seg_indptr, float global_scale,
                             void* out_q, void* out_scales, int32_t* dev_status);
+
+// Fused route + dispatch for small batches (one kernel, one block per token).
+constexpr int64_t kFusedMaxPairs = 4096;
+constexpr int64_t kFusedMaxTokens = 1024;
+bool route_dispatch_fusable(int64_t T, int K);
+cudaError_t launch_route_dispatch_small(const LaunchCtx& ctx, int mode, int quant, const uint16_t* x,
+                                        int64_t T, int H, const int32_t* topk_ids, int K, int E, int P,
+                                        int M, float global_scale, int64_t* seg_indptr, int32_t* src2dst,
+                                        int32_t* reorder_topk_ids, int32_t* masked_m,
+                                        int32_t* partition_counts, void* out_q, void* out_scales,
+                                        int32_t* dev_status);
+
+// Per-partition layout and the FlashInfer all-to-all layout (partitioned.cu).
+constexpr int kMaxPartitionsA2A = 32;
+cudaError_t launch_dispatch_layout(const LaunchCtx& ctx, const int32_t* ids, int64_t T, int K, int E, int P,
+                                   int32_t* num_tokens_per_rank, uint8_t* is_token_in_rank,
+                                   int32_t* num_tokens_per_expert, int32_t* dev_status);
+cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const uint16_t* x, int64_t T, int64_t S,
+                                        int H, const int32_t* ids, const float* w, int K, int E, int P,
+                                        int32_t invalid_id, float g, void* recv_x, uint8_t* recv_sf,
+                                        int32_t* recv_ids, float* recv_w, int32_t* dev_status);
+cudaError_t launch_combine_partitioned(const LaunchCtx& ctx, const uint16_t* partial, int64_t T, int64_t S, int H,
+                                       const int32_t* ids, int K, int E, int P, uint16_t* out, int32_t* dev_status);
 
 cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t n, uint8_t* e4m3,
                                  uint8_t* e2m1, float* e4m3_value);

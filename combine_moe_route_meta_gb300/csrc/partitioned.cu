@@ -1,0 +1,290 @@
+// partitioned.cu -- per-partition routing layout and the FlashInfer all-to-all layout.
+//
+// moe_dispatch_layout: buffer.get_dispatch_layout(topk_ids, num_experts) of
+//   _DeepEPDispatcherImplNormal._dispatch_core ("sglang token_dispatcher/deepep.py" page):
+//   is_token_in_rank [T, P], num_tokens_per_rank [P], num_tokens_per_expert [E], with the
+//   E experts split into P partitions of E/P.
+// moe_dispatch_partitioned / moe_combine_partitioned: FlashinferDispatcher.dispatch and
+//   .combine ("sglang token_dispatcher/flashinfer.py" page) for one source rank. The
+//   payload (bf16 row, or NVFP4 codes + e4m3 block scales, plus topk_ids and topk_weights)
+//   goes once to each partition owning one of the token's experts, into
+//   [P, num_slots, .] receive rows (slot = token index; num_slots plays
+//   runtime_max_tokens_per_rank). Receive ids of experts the partition does not own, of
+//   tokens it does not receive and of padding slots are set to invalid_expert_id. The
+//   combine sums, per token, the (already weighted) partial outputs of the partitions the
+//   token was sent to.
+//
+// Design: the same warp-per-(token, 512-column slice) structure as dispatch.cu / combine.cu.
+// Lanes 0..K-1 hold the token's expert ids; lane p (< P <= 32) tests every id against its
+// partition's expert range, so the destination row of lane p is p*num_slots + t or -1,
+// and the row broadcast of the shared quantise_store serves P candidate rows.
+#include <cstdint>
+
+#include "dispatch_slice.cuh"
+#include "moe_device.cuh"
+#include "moe_launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSlice = 512;
+constexpr int kLaneElems = 16;
+
+// ---------------------------------------------------------------------------
+// layout: one thread per token
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) dispatch_layout_kernel(const int32_t* __restrict__ ids, int64_t T,
+                                                                    int K, int E, int P, int32_t* ntr,
+                                                                    uint8_t* itr, int32_t* nte, int32_t* status) {
+    extern __shared__ int s_cnt[];  // [P] tokens per partition, then [E] pairs per expert
+    pdl_launch_dependents();
+    pdl_wait();
+    int* s_rank = s_cnt;
+    int* s_exp = s_cnt + P;
+    for (int j = threadIdx.x; j < P + E; j += blockDim.x) s_cnt[j] = 0;
+    __syncthreads();
+    const int ep = E / P;
+    bool bad = false;
+    for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < T; t += int64_t(gridDim.x) * blockDim.x) {
+        uint8_t* row = itr + t * P;
+        for (int p = 0; p < P; p++) row[p] = 0;
+        for (int k = 0; k < K; k++) {
+            const int e = __ldg(ids + t * K + k);
+            if (e < 0 || e >= E) {
+                bad |= e != -1;
+                continue;
+            }
+            atomicAdd(&s_exp[e], 1);
+            const int p = e / ep;
+            bool seen = false;  // an earlier slot of this token in the same partition
+            for (int k2 = 0; k2 < k; k2++) {
+                const int e2 = __ldg(ids + t * K + k2);
+                seen |= e2 >= 0 && e2 < E && e2 / ep == p;
+            }
+            if (!seen) {
+                row[p] = 1;
+                atomicAdd(&s_rank[p], 1);
+            }
+        }
+    }
+    if (__any_sync(kFullMask, bad) && (threadIdx.x & 31) == 0) set_status(status, MOE_ERR_BAD_EXPERT_ID);
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x)
+        if (s_rank[p]) atomicAdd(ntr + p, s_rank[p]);
+    if (nte != nullptr)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            if (s_exp[e]) atomicAdd(nte + e, s_exp[e]);
+}
+
+struct PartArgs {
+    const uint16_t* x;
+    const int32_t* ids;
+    const float* w;
+    int64_t T, S;  // tokens, slots per partition
+    int H, K, E, P, ep;
+    int32_t invalid_id;
+    float g;
+    void* recv_x;
+    uint8_t* recv_sf;
+    int32_t* recv_ids;
+    float* recv_w;
+    const uint16_t* partial;
+    uint16_t* out;
+    int32_t* status;
+    int units_per_row;
+    int64_t n_units;
+};
+
+// lane p: whether token t sends to partition p; all lanes return the same K ids in e_out
+__device__ __forceinline__ bool token_in_partition(const PartArgs& a, int64_t t, int lane, int& my_id) {
+    my_id = lane < a.K ? __ldg(a.ids + t * a.K + lane) : -1;
+    bool routed = false;
+    for (int k = 0; k < a.K; k++) {
+        const int e = __shfl_sync(kFullMask, my_id, k);
+        routed |= e >= 0 && e < a.E && e / a.ep == lane;
+    }
+    return routed && lane < a.P;
+}
+
+template <int QUANT>
+__global__ void __launch_bounds__(kThreads) dispatch_partitioned_kernel(PartArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int H = a.H;
+    for (int64_t u = warp; u < a.n_units; u += nwarps) {
+        const int64_t t = u / a.units_per_row;
+        const int slice = int(u - t * a.units_per_row);
+        const int col = slice * kSlice + lane * kLaneElems;
+        const bool active = col < H;
+        LaneSlice sl{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        if (active) sl = load_slice(a.x + t * H + col);
+        int my_id;
+        const bool routed = token_in_partition(a, t, lane, my_id);
+        const int64_t my_row = routed ? int64_t(lane) * a.S + t : -1;
+        if (slice == 0) {
+            // the sanitised ids and the weights of every partition's receive row
+            const float my_w = lane < a.K ? __ldg(a.w + t * a.K + lane) : 0.0f;
+            const bool valid = my_id >= 0 && my_id < a.E;
+            if (!valid && my_id != -1 && lane < a.K) set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
+            for (int p = 0; p < a.P; p++) {
+                const bool rp = __shfl_sync(kFullMask, routed, p);
+                if (lane < a.K) {
+                    const int64_t r = (int64_t(p) * a.S + t) * a.K + lane;
+                    a.recv_ids[r] = (rp && valid && my_id / a.ep == p) ? my_id : a.invalid_id;
+                    if (rp) a.recv_w[r] = my_w;
+                }
+            }
+        }
+        if constexpr (QUANT == MOE_QUANT_NVFP4_B16)
+            quantise_store<QUANT>(sl, active, lane, col, H, a.P, my_row, a.g, a.recv_x, a.recv_sf);
+        else
+            quantise_store<QUANT>(sl, active, lane, col, H, a.P, my_row, a.g, a.recv_x, nullptr);
+    }
+    // padding slots t in [T, S): every partition's ids are the invalid id
+    const int64_t pad = (a.S - a.T) * a.P * a.K;
+    for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < pad; j += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t per_p = (a.S - a.T) * a.K;
+        const int64_t p = j / per_p, rem = j - p * per_p;
+        a.recv_ids[(p * a.S + a.T) * a.K + rem] = a.invalid_id;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+    const int H = a.H;
+    constexpr int kBatch = 8;
+    for (int64_t u = warp; u < a.n_units; u += nwarps) {
+        const int64_t t = u / a.units_per_row;
+        const int col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
+        const bool active = col < H;
+        int my_id;
+        const bool routed = token_in_partition(a, t, lane, my_id);
+        const int64_t my_row = routed ? int64_t(lane) * a.S + t : -1;
+        float acc[kLaneElems];
+#pragma unroll
+        for (int j = 0; j < kLaneElems; j++) acc[j] = 0.0f;
+        for (int p0 = 0; p0 < a.P; p0 += kBatch) {
+            int64_t rows[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                rows[j] = __shfl_sync(kFullMask, my_row, (p0 + j) & 31);
+                if (p0 + j >= a.P || !active) rows[j] = -1;
+            }
+            uint4 v[kBatch][2];
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                if (rows[j] >= 0) {
+                    const uint16_t* src = a.partial + rows[j] * H + col;
+                    v[j][0] = ld_stream_v4(src);
+                    v[j][1] = ld_stream_v4(src + 8);
+                } else {
+                    v[j][0] = make_uint4(0, 0, 0, 0);
+                    v[j][1] = v[j][0];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) {
+                if (rows[j] >= 0) {
+                    float f[16];
+                    unpack8(v[j][0], f);
+                    unpack8(v[j][1], f + 8);
+#pragma unroll
+                    for (int e = 0; e < kLaneElems; e++) acc[e] += f[e];
+                }
+            }
+        }
+        if (active) {
+            uint16_t* dst = a.out + t * H + col;
+            st_v4(dst, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+            st_v4(dst + 8, make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                      pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
+        }
+    }
+}
+
+template <typename Kernel>
+cudaError_t launch_units(const LaunchCtx& ctx, Kernel kern, const PartArgs& a, int64_t extra_threads) {
+    int per_sm = 0;
+    cudaError_t err = blocks_per_sm(ctx, kern, kThreads, 0, &per_sm);
+    if (err != cudaSuccess) return err;
+    const int64_t need = std::max((a.n_units * 32 + kThreads - 1) / kThreads, (extra_threads + kThreads - 1) / kThreads);
+    const int64_t cap = int64_t(ctx.num_sms) * per_sm;
+    const int grid = int(std::max<int64_t>(1, std::min(need, cap)));
+    return launch_pdl(ctx, kern, dim3(grid), dim3(kThreads), 0, a);
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_layout(const LaunchCtx& ctx, const int32_t* ids, int64_t T, int K, int E, int P,
+                                   int32_t* num_tokens_per_rank, uint8_t* is_token_in_rank,
+                                   int32_t* num_tokens_per_expert, int32_t* dev_status) {
+    cudaError_t err = cudaMemsetAsync(num_tokens_per_rank, 0, sizeof(int32_t) * size_t(P), ctx.stream);
+    if (err == cudaSuccess && num_tokens_per_expert)
+        err = cudaMemsetAsync(num_tokens_per_expert, 0, sizeof(int32_t) * size_t(E), ctx.stream);
+    if (err != cudaSuccess || T == 0) return err;
+    const int64_t blocks = std::min<int64_t>((T + kThreads - 1) / kThreads, int64_t(ctx.num_sms) * 4);
+    return launch_pdl(ctx, dispatch_layout_kernel, dim3(int(blocks)), dim3(kThreads),
+                      sizeof(int) * size_t(P + E), ids, T, K, E, P, num_tokens_per_rank, is_token_in_rank,
+                      num_tokens_per_expert, dev_status);
+}
+
+cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const uint16_t* x, int64_t T, int64_t S,
+                                        int H, const int32_t* ids, const float* w, int K, int E, int P,
+                                        int32_t invalid_id, float g, void* recv_x, uint8_t* recv_sf,
+                                        int32_t* recv_ids, float* recv_w, int32_t* dev_status) {
+    PartArgs a{};
+    a.x = x;
+    a.ids = ids;
+    a.w = w;
+    a.T = T;
+    a.S = S;
+    a.H = H;
+    a.K = K;
+    a.E = E;
+    a.P = P;
+    a.ep = E / P;
+    a.invalid_id = invalid_id;
+    a.g = g;
+    a.recv_x = recv_x;
+    a.recv_sf = recv_sf;
+    a.recv_ids = recv_ids;
+    a.recv_w = recv_w;
+    a.status = dev_status;
+    a.units_per_row = (H + kSlice - 1) / kSlice;
+    a.n_units = T * a.units_per_row;
+    const int64_t pad = (S - T) * P * K;
+    if (a.n_units == 0 && pad == 0) return cudaSuccess;
+    if (quant == MOE_QUANT_NVFP4_B16) return launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NVFP4_B16>, a, pad);
+    return launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NONE>, a, pad);
+}
+
+cudaError_t launch_combine_partitioned(const LaunchCtx& ctx, const uint16_t* partial, int64_t T, int64_t S, int H,
+                                       const int32_t* ids, int K, int E, int P, uint16_t* out, int32_t* dev_status) {
+    PartArgs a{};
+    a.partial = partial;
+    a.ids = ids;
+    a.T = T;
+    a.S = S;
+    a.H = H;
+    a.K = K;
+    a.E = E;
+    a.P = P;
+    a.ep = E / P;
+    a.out = out;
+    a.status = dev_status;
+    a.units_per_row = (H + kSlice - 1) / kSlice;
+    a.n_units = T * a.units_per_row;
+    if (a.n_units == 0) return cudaSuccess;
+    return launch_units(ctx, combine_partitioned_kernel, a, 0);
+}
+
+}  // namespace moe

@@ -19,12 +19,13 @@
 //    block ranks and gives the block's histogram.
 //  * One block (n_pairs <= 8192): block-wide scan of the histogram -> seg_indptr, and
 //    the final positions are written in the same kernel.
-//  * Several blocks: each block publishes its histogram row to a [B][E] table and
-//    writes block ranks into src2dst. The last block to finish (atomic ticket,
-//    threadfence pattern -- no block ever waits for another) scans the table column
-//    by column into per-block expert offsets and scans the totals into seg_indptr.
-//    A second kernel adds seg_indptr[e] + offset[b][e] to every rank and scatters
-//    reorder_topk_ids. Nothing spins, so no wait needs a bound.
+//  * Several blocks: each block publishes its histogram row to a [B][E] table and writes
+//    block ranks into src2dst. A second kernel (launched as a programmatic dependent)
+//    gives every block the whole table in one batch of L2 loads: the column sums over
+//    the rows before its own are its per-expert offsets, the full column sums scanned
+//    over the experts are seg_indptr (block 0 writes the per-expert outputs); it then
+//    finalises its own pairs. No block ever waits for another, so nothing spins.
+#include <algorithm>
 #include <cstdint>
 
 #include "moe_device.cuh"
@@ -35,7 +36,7 @@ namespace {
 
 constexpr int kWarps = kRouteThreads / 32;
 
-// workspace layout: [0] ticket (uint32), table at byte offset 256: int32 [B][E]
+// workspace layout: a 256-byte reserved header, then the int32 table [B][E]
 constexpr size_t kTableOffset = 256;
 
 // Block-wide exclusive scan of one int per thread (blockDim == 1024).
@@ -68,48 +69,60 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 
 // Final per-expert outputs from the histogram held in shared memory.
 // hist[e] (e < E) -> seg (shared, E+1 ints), seg_indptr, masked_m, partition_counts.
+// With `write` false only the shared seg[] is produced.
 __device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int E, int P, int M,
                                  int64_t* seg_indptr, int32_t* masked_m, int32_t* partition_counts,
-                                 int32_t* status) {
+                                 int32_t* status, bool write = true) {
     const int e = threadIdx.x;  // E <= 1024 == blockDim
     const int c = e < E ? hist[e] : 0;
     int total;
     const int excl = block_exclusive_scan(c, warp_sums, &total);
     if (e < E) {
         seg[e] = excl;
-        seg_indptr[e] = excl;
-        int mm = c;
-        if (M > 0 && c > M) {
-            mm = M;
-            set_status(status, MOE_ERR_CAPACITY);
+        if (write) {
+            seg_indptr[e] = excl;
+            int mm = c;
+            if (M > 0 && c > M) {
+                mm = M;
+                set_status(status, MOE_ERR_CAPACITY);
+            }
+            masked_m[e] = mm;
         }
-        masked_m[e] = mm;
     }
     if (e == 0) {
         seg[E] = total;
-        seg_indptr[E] = total;
+        if (write) seg_indptr[E] = total;
     }
     __syncthreads();
-    if (partition_counts != nullptr && e < P) {
+    if (write && partition_counts != nullptr && e < P) {
         const int ep = E / P;
         partition_counts[e] = seg[(e + 1) * ep] - seg[e * ep];
     }
 }
 
+// Row stride of the per-warp counter table cnt[32][S]: odd, so the 32 lanes of a warp
+// reading one expert's column (lane l -> row l) hit 32 different banks.
+__host__ __device__ constexpr int cnt_stride(int E) { return E | 1; }
+
+// A pair's expert and in-warp rank packed in one register: rank (< 32*16) above bit 11,
+// expert + 1 (0 = no valid expert, E <= 1024) in the low 11 bits.
+__device__ __forceinline__ int pack_er(int e, int rank) { return (rank << 11) | (e + 1); }
+__device__ __forceinline__ int er_expert(int p) { return (p & 0x7ff) - 1; }
+__device__ __forceinline__ int er_rank(int p) { return p >> 11; }
+
 // Phase 1 of every block: per-warp stable ranks and per-warp counters.
-// cnt: shared [32][E]. Fills e_r / rank_r for the R rounds of this thread.
+// cnt: shared [32][S]. Fills er[r] (packed expert, rank) for the R rounds of this thread.
 template <int RMAX>
 __device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, int64_t n_pairs, int E,
-                                           int R, int64_t warp_base, int* cnt, int (&e_r)[RMAX],
-                                           int (&rank_r)[RMAX], int32_t* status) {
+                                           int R, int64_t warp_base, int* cnt, int (&er)[RMAX],
+                                           int32_t* status) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const unsigned lt = (1u << lane) - 1u;
-    int* my = cnt + w * E;
+    int* my = cnt + w * cnt_stride(E);
     bool bad = false;
 #pragma unroll
     for (int r = 0; r < RMAX; r++) {
-        e_r[r] = -1;
-        rank_r[r] = 0;
+        er[r] = pack_er(-1, 0);
         if (r < R) {
             const int64_t i = warp_base + r * 32 + lane;
             int e = -1;
@@ -127,24 +140,28 @@ __device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, int6
             __syncwarp();
             if (e >= 0 && lane == __ffs(peers) - 1) my[e] = base + __popc(peers);
             __syncwarp();
-            e_r[r] = e;
-            rank_r[r] = base + __popc(peers & lt);
+            er[r] = pack_er(e, base + __popc(peers & lt));
         }
     }
     if (__any_sync(kFullMask, bad) && lane == 0) set_status(status, MOE_ERR_BAD_EXPERT_ID);
 }
 
-// Exclusive scan of cnt[w][e] over the 32 warps, per expert; returns block totals in hist.
+// Exclusive scan of cnt[w][e] over the 32 warps, per expert; block totals go to hist.
+// Warp v scans the columns e = v, v+32, ...: lane l holds warp l's count, a 5-step
+// shuffle scan gives every lane its exclusive prefix, lane 31 the column total.
 __device__ __forceinline__ void scan_warps(int* cnt, int* hist, int E) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-#pragma unroll 8
-        for (int w = 0; w < kWarps; w++) {
-            const int c = cnt[w * E + e];
-            cnt[w * E + e] = run;
-            run += c;
+    const int lane = threadIdx.x & 31, v = threadIdx.x >> 5;
+    const int S = cnt_stride(E);
+    for (int e = v; e < E; e += kWarps) {
+        const int c = cnt[lane * S + e];
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFullMask, x, o);
+            if (lane >= o) x += y;
         }
-        hist[e] = run;
+        cnt[lane * S + e] = x - c;
+        if (lane == 31) hist[e] = x;
     }
 }
 
@@ -157,14 +174,13 @@ struct RouteArgs {
     int32_t* reorder;
     int32_t* masked_m;
     int32_t* partition_counts;
-    unsigned* ticket;
     int32_t* table;  // [B][E]
     int32_t* status;
 };
 
-// shared memory: cnt[32][E] | hist[E] | seg[E+1] | warp_sums[32] | flag
+// shared memory: cnt[32][S] | hist[E] | seg[E+1] | warp_sums[32] | one spare int
 __host__ __device__ constexpr size_t route_smem_bytes(int E) {
-    return sizeof(int) * (size_t(kWarps) * E + E + (E + 1) + 32 + 1);
+    return sizeof(int) * (size_t(kWarps) * cnt_stride(E) + E + (E + 1) + 32 + 1);
 }
 
 // One block for all pairs.
@@ -172,18 +188,20 @@ template <int RMAX>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_single_kernel(RouteArgs a) {
     extern __shared__ int smem[];
     const int E = a.E;
+    const int S = cnt_stride(E);
     int* cnt = smem;
-    int* hist = cnt + kWarps * E;
+    int* hist = cnt + kWarps * S;
     int* seg = hist + E;
     int* warp_sums = seg + E + 1;
-    for (int j = threadIdx.x; j < kWarps * E; j += blockDim.x) cnt[j] = 0;
+    for (int j = threadIdx.x; j < kWarps * S; j += blockDim.x) cnt[j] = 0;
     __syncthreads();
     pdl_launch_dependents();
+    pdl_wait();
 
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t warp_base = int64_t(w) * 32 * a.R;
-    int e_r[RMAX], rank_r[RMAX];
-    warp_ranks<RMAX>(a.ids, a.n_pairs, E, a.R, warp_base, cnt, e_r, rank_r, a.status);
+    int er[RMAX];
+    warp_ranks<RMAX>(a.ids, a.n_pairs, E, a.R, warp_base, cnt, er, a.status);
     __syncthreads();
     scan_warps(cnt, hist, E);
     __syncthreads();
@@ -195,9 +213,9 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_single_kernel(Rou
         if (r < a.R) {
             const int64_t i = warp_base + r * 32 + lane;
             if (i < a.n_pairs) {
-                const int e = e_r[r];
+                const int e = er_expert(er[r]);
                 if (e >= 0) {
-                    const int d = seg[e] + cnt[w * E + e] + rank_r[r];
+                    const int d = seg[e] + cnt[w * S + e] + er_rank(er[r]);
                     a.src2dst[i] = d;
                     a.reorder[d] = e;
                 } else {
@@ -208,25 +226,24 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_single_kernel(Rou
     }
 }
 
-// Several blocks, kernel 1: block ranks + histogram rows; the last block scans.
+// Several blocks, kernel 1: block ranks + histogram rows.
 template <int RMAX>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_count_kernel(RouteArgs a) {
     extern __shared__ int smem[];
     const int E = a.E;
+    const int S = cnt_stride(E);
     int* cnt = smem;
-    int* hist = cnt + kWarps * E;
-    int* seg = hist + E;
-    int* warp_sums = seg + E + 1;
-    int* flag = warp_sums + 32;
-    for (int j = threadIdx.x; j < kWarps * E; j += blockDim.x) cnt[j] = 0;
+    int* hist = cnt + kWarps * S;
+    for (int j = threadIdx.x; j < kWarps * S; j += blockDim.x) cnt[j] = 0;
     __syncthreads();
+    pdl_launch_dependents();  // the place kernel may start launching (it waits for us)
+    pdl_wait();
 
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int B = gridDim.x;
     const int64_t block_base = int64_t(blockIdx.x) * kRouteThreads * a.R;
     const int64_t warp_base = block_base + int64_t(w) * 32 * a.R;
-    int e_r[RMAX], rank_r[RMAX];
-    warp_ranks<RMAX>(a.ids, a.n_pairs, E, a.R, warp_base, cnt, e_r, rank_r, a.status);
+    int er[RMAX];
+    warp_ranks<RMAX>(a.ids, a.n_pairs, E, a.R, warp_base, cnt, er, a.status);
     __syncthreads();
     scan_warps(cnt, hist, E);
     __syncthreads();
@@ -235,65 +252,78 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_count_kernel(Rout
     for (int r = 0; r < RMAX; r++) {
         if (r < a.R) {
             const int64_t i = warp_base + r * 32 + lane;
-            if (i < a.n_pairs) a.src2dst[i] = e_r[r] >= 0 ? cnt[w * E + e_r[r]] + rank_r[r] : -1;
+            const int e = er_expert(er[r]);
+            if (i < a.n_pairs) a.src2dst[i] = e >= 0 ? cnt[w * S + e] + er_rank(er[r]) : -1;
         }
     }
-
-    // ---- last block: column scan of the [B][E] table, then seg_indptr ----
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) *flag = (atomicInc(a.ticket, unsigned(B - 1)) == unsigned(B - 1));
-    __syncthreads();
-    if (!*flag) return;
-    __threadfence();
-
-    // G threads per expert column, each owning a contiguous run of rows; G <= 32 keeps
-    // the partial sums [G][E] inside the cnt[32][E] region they reuse.
-    const int G = min(kRouteThreads / E, kWarps);  // >= 1
-    const int rows_per = (B + G - 1) / G;
-    int* part = cnt;  // reuse: [G][E]
-    const int tid = threadIdx.x;
-    const int col = tid % E, g = tid / E;
-    const bool active = tid < G * E;
-    const int b0 = g * rows_per, b1 = min(B, b0 + rows_per);
-    int psum = 0;
-    if (active) {
-        for (int b = b0; b < b1; b++) psum += __ldcg(a.table + size_t(b) * E + col);
-        part[g * E + col] = psum;
-    }
-    __syncthreads();
-    if (active) {
-        int off = 0;
-        for (int g2 = 0; g2 < g; g2++) off += part[g2 * E + col];
-        for (int b = b0; b < b1; b++) {
-            int32_t* p = a.table + size_t(b) * E + col;
-            const int v = __ldcg(p);
-            __stcg(p, off);
-            off += v;
-        }
-        if (g == G - 1) hist[col] = off;  // column total
-    }
-    __syncthreads();
-    finish_histogram(hist, seg, warp_sums, E, a.P, a.M, a.seg_indptr, a.masked_m,
-                     a.partition_counts, a.status);
 }
 
-// Several blocks, kernel 2: final positions.
+// Several blocks, kernel 2: column sums of the table -> offsets and seg_indptr; final positions.
+// shared memory: part_pre[G][E] | part_tot[G][E] | tot[E] | pre[E] | seg[E+1] | warp_sums[32]
 __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteArgs a) {
-    extern __shared__ int base[];  // [E]
+    extern __shared__ int smem[];
+    pdl_launch_dependents();
     pdl_wait();
-    const int E = a.E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        base[e] = int(a.seg_indptr[e]) + __ldcg(a.table + size_t(blockIdx.x) * E + e);
-    if (blockIdx.x == 0 && threadIdx.x == 0) *a.ticket = 0u;
+    const int E = a.E, B = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
+    const int G = min(kRouteThreads / E, kWarps);  // threads per column
+    int* part_pre = smem;
+    int* part_tot = part_pre + G * E;
+    int* tot = part_tot + G * E;
+    int* pre = tot + E;
+    int* seg = pre + E;
+    int* warp_sums = seg + E + 1;
+
+    // this thread's first pair (in-block rank and expert) is fetched before the table work
+    const int64_t i0 = int64_t(b) * kRouteThreads * a.R;
+    const int64_t i1 = min(a.n_pairs, i0 + int64_t(kRouteThreads) * a.R);
+    int d_first = -1, e_first = -1;
+    if (i0 + tid < i1) {
+        d_first = a.src2dst[i0 + tid];
+        e_first = __ldg(a.ids + i0 + tid);
+    }
+
+    // every block reads the whole table: G threads per column, each a contiguous run of
+    // rows fetched kColBatch loads at a time
+    constexpr int kColBatch = 16;
+    const int rows_per = (B + G - 1) / G;
+    const int col = tid % E, g = tid / E;
+    if (tid < G * E) {
+        const int b0 = g * rows_per, b1 = min(B, b0 + rows_per);
+        int p = 0, q = 0;
+        for (int c0 = b0; c0 < b1; c0 += kColBatch) {
+            int v[kColBatch];
+#pragma unroll
+            for (int j = 0; j < kColBatch; j++)
+                v[j] = c0 + j < b1 ? __ldcg(a.table + size_t(c0 + j) * E + col) : 0;
+#pragma unroll
+            for (int j = 0; j < kColBatch; j++) {
+                q += v[j];
+                p += c0 + j < b ? v[j] : 0;
+            }
+        }
+        part_pre[g * E + col] = p;
+        part_tot[g * E + col] = q;
+    }
     __syncthreads();
-    const int64_t b0 = int64_t(blockIdx.x) * kRouteThreads * a.R;
-    const int64_t b1 = min(a.n_pairs, b0 + int64_t(kRouteThreads) * a.R);
-    for (int64_t i = b0 + threadIdx.x; i < b1; i += blockDim.x) {
-        const int d = a.src2dst[i];
+    if (tid < E) {
+        int p = 0, q = 0;
+        for (int g2 = 0; g2 < G; g2++) {
+            p += part_pre[g2 * E + tid];
+            q += part_tot[g2 * E + tid];
+        }
+        pre[tid] = p;
+        tot[tid] = q;
+    }
+    __syncthreads();
+    finish_histogram(tot, seg, warp_sums, E, a.P, a.M, a.seg_indptr, a.masked_m, a.partition_counts,
+                     a.status, b == 0);
+
+    for (int64_t i = i0 + tid; i < i1; i += blockDim.x) {
+        const bool first = i == i0 + tid;
+        const int d = first ? d_first : a.src2dst[i];
+        const int e = first ? e_first : __ldg(a.ids + i);
         if (d >= 0) {
-            const int e = __ldg(a.ids + i);
-            const int dst = base[e] + d;
+            const int dst = seg[e] + pre[e] + d;
             a.src2dst[i] = dst;
             a.reorder[dst] = e;
         }
@@ -309,31 +339,19 @@ cudaError_t launch_rmax(const LaunchCtx& ctx, const RoutePlan& plan, const Route
             cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
             if (err != cudaSuccess) return err;
         }
-        k<<<1, kRouteThreads, smem, ctx.stream>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(ctx, k, dim3(1), dim3(kRouteThreads), smem, a);
     }
     auto k1 = route_meta_count_kernel<RMAX>;
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err != cudaSuccess) return err;
     }
-    k1<<<plan.blocks, kRouteThreads, smem, ctx.stream>>>(a);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(ctx, k1, dim3(plan.blocks), dim3(kRouteThreads), smem, a);
     if (err != cudaSuccess) return err;
-
-    // kernel 2 as a programmatic dependent: its launch overlaps kernel 1's tail and
-    // griddepcontrol.wait orders every read after kernel 1's writes.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.blocks);
-    cfg.blockDim = dim3(kRouteThreads);
-    cfg.dynamicSmemBytes = sizeof(int) * size_t(E);
-    cfg.stream = ctx.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, route_meta_place_kernel, a);
+    // kernel 2's launch overlaps kernel 1's tail; griddepcontrol.wait orders its reads
+    const int G = std::min(kRouteThreads / E, kWarps);
+    const size_t smem2 = sizeof(int) * (size_t(2 * G) * E + 3 * size_t(E) + 1 + 32);
+    return launch_pdl(ctx, route_meta_place_kernel, dim3(plan.blocks), dim3(kRouteThreads), smem2, a);
 }
 
 }  // namespace
@@ -377,10 +395,7 @@ cudaError_t launch_route_meta(const LaunchCtx& ctx, const RoutePlan& plan, const
     a.masked_m = masked_m;
     a.partition_counts = partition_counts;
     a.status = dev_status;
-    if (!plan.single) {
-        a.ticket = static_cast<unsigned*>(workspace);
-        a.table = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kTableOffset);
-    }
+    if (!plan.single) a.table = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kTableOffset);
     if (plan.rounds <= 1) return launch_rmax<1>(ctx, plan, a, E);
     if (plan.rounds <= 2) return launch_rmax<2>(ctx, plan, a, E);
     if (plan.rounds <= 4) return launch_rmax<4>(ctx, plan, a, E);

@@ -199,6 +199,29 @@ moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t *hi
                           void *out_scales, int32_t *dev_status, moe_stream_t stream);
 
 /*
+ * moe_route_dispatch -- moe_route_meta followed by moe_dispatch, in one call.
+ *
+ * Same results as the two calls (all their outputs are written), for the dispatch
+ * sequence of _DeepEPDispatcherImplNormal._deepep_permute (diff page: preprocess, then
+ * PreReorder) and of low_latency_dispatch (deepep.py page: counts and the masked layout in
+ * one step). Arguments are the union of the two calls' arguments, with the same meaning
+ * and limits; max_tokens_per_expert is the masked capacity (>= 1 in masked mode; >= 0 in
+ * normal mode, where M > 0 only enables the capacity check of masked_m).
+ * Small batches (T <= 1024 and T*K <= 4096 pairs) run as a single kernel that needs no
+ * workspace (workspace may be NULL); larger ones need moe_route_meta_workspace_size(T, K, E)
+ * bytes of zero-filled workspace, exactly as moe_route_meta.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
+ */
+moe_status_t moe_route_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t *hidden_states,
+                                int64_t num_tokens, int hidden, const int32_t *topk_ids, int topk,
+                                int num_experts, int num_partitions, int max_tokens_per_expert,
+                                float input_global_scale, int64_t *seg_indptr, int32_t *src2dst,
+                                int32_t *reorder_topk_ids, int32_t *masked_m,
+                                int32_t *partition_counts, int32_t *expected_m_host, void *workspace,
+                                size_t workspace_bytes, void *out_q, void *out_scales,
+                                int32_t *dev_status, moe_stream_t stream);
+
+/*
  * moe_combine -- weighted reduction of expert outputs back to token order.
  *
  * Operation (deepep_post_reorder in combine_a on the diff page; low_latency_combine in
@@ -221,6 +244,67 @@ moe_status_t moe_combine(moe_mode_t mode, const uint16_t *expert_out, int64_t nu
                          const int32_t *topk_ids, const int32_t *src2dst,
                          const int64_t *seg_indptr, const float *topk_weights, uint16_t *out,
                          int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_dispatch_layout -- which expert-parallel partitions each token is sent to.
+ *
+ * buffer.get_dispatch_layout(topk_ids, num_experts) in _DeepEPDispatcherImplNormal._dispatch_core
+ * ("sglang token_dispatcher/deepep.py" page), with the E experts split into P partitions
+ * of E/P consecutive experts (the RDMA-rank counts of the inter-node transport have no
+ * counterpart on one GPU):
+ *   is_token_in_rank[t][p]   = 1 iff some valid slot of token t names an expert of p
+ *   num_tokens_per_rank[p]   = #{t : is_token_in_rank[t][p]}
+ *   num_tokens_per_expert[e] = #{valid (t, k) with topk_ids[t][k] = e}
+ * Arguments: topk_ids [T, K] int32; num_partitions (P) >= 1 with E % P == 0;
+ * num_tokens_per_rank [P] int32 out; is_token_in_rank [T, P] uint8 out (0/1);
+ * num_tokens_per_expert [E] int32 out or NULL. Ids outside [-1, E) are skipped and reported
+ * as MOE_ERR_BAD_EXPERT_ID in *dev_status. The counts are cleared on `stream` first.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
+ */
+moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int64_t num_tokens, int topk, int num_experts,
+                                 int num_partitions, int32_t *num_tokens_per_rank,
+                                 uint8_t *is_token_in_rank, int32_t *num_tokens_per_expert,
+                                 int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_dispatch_partitioned -- the FlashInfer all-to-all dispatch layout, one source rank.
+ *
+ * FlashinferDispatcher.dispatch ("sglang token_dispatcher/flashinfer.py" page): the payload
+ * [x or its NVFP4 codes, NVFP4 block scales, topk_ids, topk_weights] of token t goes once to
+ * every partition p that owns one of its experts, into slot t of p's receive rows:
+ *   recv_x[p][t]             = hidden_states[t] (bf16) or its NVFP4 codes (as moe_dispatch)
+ *   recv_scales[p][t]        = the e4m3 block scales [H/16] (NVFP4 only)
+ *   recv_topk_ids[p][t][k]   = topk_ids[t][k] if that expert belongs to p, else invalid_expert_id
+ *   recv_topk_weights[p][t][k] = topk_weights[t][k]
+ * Slots of tokens p does not receive, and padding slots t in [T, num_slots), get
+ * invalid_expert_id in every recv_topk_ids entry; their other payload is left untouched.
+ * num_slots plays runtime_max_tokens_per_rank (>= T). quant: MOE_QUANT_NONE or
+ * MOE_QUANT_NVFP4_B16 (input_global_scale as in moe_dispatch). Limits: P <= 32, H % 16 == 0,
+ * hidden_states / recv_x 16-byte aligned. Shapes: recv_x [P, num_slots, H] bf16 or
+ * [P, num_slots, H/2] uint8; recv_scales [P, num_slots, H/16]; recv_topk_ids / weights
+ * [P, num_slots, K].
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
+ */
+moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t *hidden_states, int64_t num_tokens,
+                                      int64_t num_slots, int hidden, const int32_t *topk_ids,
+                                      const float *topk_weights, int topk, int num_experts, int num_partitions,
+                                      int32_t invalid_expert_id, float input_global_scale, void *recv_x,
+                                      uint8_t *recv_scales, int32_t *recv_topk_ids, float *recv_topk_weights,
+                                      int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_combine_partitioned -- the FlashInfer all-to-all combine, one source rank.
+ *
+ * FlashinferDispatcher.combine (flashinfer.py page): each partition's output rows
+ * [P, num_slots, H] bf16 (already weighted by its experts) are summed back per token over
+ * the partitions the token was sent to, in ascending p, fp32 accumulation, one rounding:
+ *   out[t] = bf16_rn( sum_{p : token t sent to p} partial[p][t] ),   zeros if sent nowhere.
+ * Arguments as moe_dispatch_partitioned; out [T, H] bf16, 16-byte aligned.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
+ */
+moe_status_t moe_combine_partitioned(const uint16_t *partial, int64_t num_tokens, int64_t num_slots, int hidden,
+                                     const int32_t *topk_ids, int topk, int num_experts, int num_partitions,
+                                     uint16_t *out, int32_t *dev_status, moe_stream_t stream);
 
 /*
  * moe_convert_probe -- diagnostics: run the number-format conversions of the quantising

@@ -214,3 +214,52 @@ def test_dispatcher_graph_capture_replays_correctly():
     assert torch.equal(d.out_q, ref_q)
     assert torch.equal(d.out, ref_out)
     d.check()
+
+
+# --- moe_route_dispatch: route + dispatch in one call -------------------------------------
+
+@pytest.mark.parametrize("T,H,E,K,mode,quant,M,P", [
+    (128, 7168, 256, 8, "masked", "fp8g128", 128, 8),   # the decode shape: one fused kernel
+    (1, 16, 1, 1, "normal", "none", 0, 1),
+    (33, 272, 5, 3, "masked", "none", 9, 5),             # capacity drops inside the fused kernel
+    (100, 1040, 64, 6, "normal", "nvfp4b16", 0, 4),
+    (256, 4096, 128, 16, "masked", "nvfp4b16", 64, 8),   # 4096 pairs: the largest fused batch
+    (1024, 128, 1024, 4, "normal", "fp8g128", 0, 2),     # 1024 tokens, E at its limit
+    (4096, 512, 256, 8, "normal", "fp8g128", 0, 8),      # beyond the fused limits: route kernels + dispatch
+    (513, 256, 16, 8, "masked", "none", 600, 4),         # 4104 pairs: just past the fused limit
+])
+def test_route_dispatch_matches_oracle(T, H, E, K, mode, quant, M, P):
+    import oracle as orc
+    from _harness import SENTINEL, check_meta, filled
+    m = moe()
+    w = make_case(T, H, E, K, seed=T * 7 + H, mode=mode, quant=quant, M=M, P=P, invalid_rate=0.05,
+                  routing="zipf" if E >= K else "replace")
+    x, ids, _ = to_dev(w)
+    d = m.MoEDispatcher(T, H, K, E, mode=mode, quant=quant, num_partitions=P, max_tokens_per_expert=M)
+    qs, qd, ss, sd = m.dispatch_out_shapes(mode, quant, T, H, K, E, M)
+    d.out_q = filled(qs, qd)
+    d.out_scales = filled(ss, sd) if ss is not None else None
+    d.route_dispatch(x, ids, w.global_scale or 0.0)
+    om = orc.route_meta(w.topk_ids, E, P=P, M=M)
+    oq, osc = orc.dispatch(mode, quant, w.x, w.topk_ids, om, E, M=M, global_scale=w.global_scale or 0.0,
+                           fill=SENTINEL)
+    torch.cuda.synchronize()
+    meta = m.RouteMeta(d.seg_indptr, d.src2dst, d.reorder_topk_ids, d.masked_m, d.partition_counts, d.expected_m)
+    check_meta(w, om, meta, d.status)
+    gq = bytes_of(d.out_q)
+    assert np.array_equal(gq, np.ascontiguousarray(oq).view(np.uint8).reshape(gq.shape))
+    if d.out_scales is not None:
+        gs = bytes_of(d.out_scales)
+        assert np.array_equal(gs, np.ascontiguousarray(osc).view(np.uint8).reshape(gs.shape))
+
+
+def test_route_dispatch_bad_ids_reported_once():
+    m = moe()
+    w = make_case(64, 256, 16, 4, seed=21, bad_rate=0.05)
+    x, ids, _ = to_dev(w)
+    d = m.MoEDispatcher(64, 256, 4, 16)
+    d.route_dispatch(x, ids)
+    torch.cuda.synchronize()
+    assert int(d.status.item()) == m.MOE_ERR_BAD_EXPERT_ID
+    om = oracle.route_meta(w.topk_ids, 16)
+    assert np.array_equal(d.src2dst.cpu().numpy(), om.src2dst)

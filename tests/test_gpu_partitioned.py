@@ -1,0 +1,111 @@
+"""GPU parity of the per-partition layout (moe_dispatch_layout) and the FlashInfer
+all-to-all layout (moe_dispatch_partitioned / moe_combine_partitioned) against the oracle.
+
+Layout, receive rows, sanitised ids, weights and NVFP4 codes/scales are compared bit for
+bit, including the payload the kernels must leave untouched; the combine within
+1e-2 relative / 1e-3 absolute.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import make_case, make_workload, random_bf16
+
+from _harness import SENTINEL, bytes_of, check_combine, filled, moe, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,E,K,P,bad", [
+    (0, 16, 4, 4, 0.0), (1, 8, 2, 1, 0.0), (300, 64, 6, 8, 0.0), (5000, 256, 8, 32, 0.02), (16384, 128, 8, 8, 0.0),
+])
+def test_dispatch_layout_matches_oracle(T, E, K, P, bad):
+    m = moe()
+    w = make_case(T, 16, E, K, seed=T + P, invalid_rate=0.05, bad_rate=bad,
+                  routing="replace" if T == 5000 else "uniform")
+    _, ids, _ = to_dev(w)
+    ntr = torch.full((P,), -1, dtype=torch.int32, device="cuda")
+    itr = torch.full((max(T, 1), P), 7, dtype=torch.uint8, device="cuda")[:T]
+    nte = torch.full((E,), -1, dtype=torch.int32, device="cuda")
+    st = m.new_status()
+    m.moe_dispatch_layout(ids, E, P, ntr, itr, st, nte)
+    o_ntr, o_itr, o_nte = oracle.dispatch_layout(w.topk_ids, E, P)
+    torch.cuda.synchronize()
+    assert np.array_equal(ntr.cpu().numpy(), o_ntr)
+    assert np.array_equal(itr.cpu().numpy().astype(bool), o_itr)
+    assert np.array_equal(nte.cpu().numpy(), o_nte)
+    assert int(st.item()) == (m.MOE_ERR_BAD_EXPERT_ID if bad else 0)
+
+
+@pytest.mark.parametrize("T,S,H,E,K,P,quant,inv", [
+    (64, 64, 256, 16, 4, 4, "none", -1),
+    (50, 61, 1040, 32, 6, 8, "nvfp4b16", 32),       # padding slots, ragged 512-slice, invalid id = E
+    (128, 128, 7168, 256, 8, 8, "nvfp4b16", -1),    # the FlashInfer NVFP4 payload shape (decode-sized)
+    (512, 600, 4096, 128, 8, 8, "none", 128),
+    (37, 37, 128, 64, 16, 32, "none", -1),          # P = 32 (one lane per partition), K = 16
+    (20, 20, 64, 4, 2, 1, "nvfp4b16", -1),          # a single partition
+])
+def test_partitioned_dispatch_and_combine_match_oracle(T, S, H, E, K, P, quant, inv):
+    m = moe()
+    w = make_case(T, H, E, K, seed=T * 3 + P, quant=quant, invalid_rate=0.05)
+    x, ids, wt = to_dev(w)
+    g = w.global_scale or 0.0
+    if quant == "nvfp4b16":
+        rx = filled((P, S, H // 2), torch.uint8)
+        rsf = filled((P, S, H // 16), torch.uint8)
+    else:
+        rx = filled((P, S, H), torch.bfloat16)
+        rsf = None
+    rids = filled((P, S, K), torch.int32)
+    rw = filled((P, S, K), torch.float32)
+    st = m.new_status()
+    m.moe_dispatch_partitioned(quant, x, ids, wt, E, P, rx, rsf, rids, rw, st, invalid_expert_id=inv,
+                               input_global_scale=g)
+    ox, osf, oids, ow = oracle.dispatch_partitioned(quant, w.x, w.topk_ids, w.topk_weights, E, P, invalid_id=inv,
+                                                    global_scale=g, num_slots=S, fill=SENTINEL)
+    torch.cuda.synchronize()
+    assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
+    if rsf is not None:
+        assert np.array_equal(bytes_of(rsf), osf.reshape(P, -1))
+    assert np.array_equal(rids.cpu().numpy(), oids)
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
+    assert int(st.item()) == 0
+
+    partial_h = random_bf16(np.random.default_rng(T + S), (P, S, H))
+    partial = torch.from_numpy(partial_h.view(np.int16)).cuda().view(torch.bfloat16)
+    out = filled((T, H), torch.bfloat16)
+    m.moe_combine_partitioned(partial, ids, E, P, out, st)
+    want = oracle.combine_partitioned(partial_h, w.topk_ids, E, P)
+    torch.cuda.synchronize()
+    check_combine(bytes_of(out).view(np.uint16).reshape(T, H), want)
+
+
+def test_partitioned_nvfp4_workload_layout_and_sampled_rows():
+    """The nvfp4 workload (T=8192, H=7168, E=256, K=8, P=8) through the FlashInfer layout:
+    sanitised ids and weights in full, NVFP4 rows on a sample of tokens."""
+    m = moe()
+    w = make_workload("nvfp4")
+    x, ids, wt = to_dev(w)
+    P, S, K, H = w.P, w.T, w.K, w.H
+    rx = torch.empty((P, S, H // 2), dtype=torch.uint8, device="cuda")
+    rsf = torch.empty((P, S, H // 16), dtype=torch.uint8, device="cuda")
+    rids = torch.empty((P, S, K), dtype=torch.int32, device="cuda")
+    rw = torch.zeros((P, S, K), dtype=torch.float32, device="cuda")
+    st = m.new_status()
+    m.moe_dispatch_partitioned("nvfp4b16", x, ids, wt, w.E, P, rx, rsf, rids, rw, st, input_global_scale=w.global_scale)
+    torch.cuda.synchronize()
+    gids = rids.cpu().numpy()
+    ep = w.E // P
+    part = np.where(w.topk_ids >= 0, w.topk_ids // ep, -1)
+    for p in range(P):
+        want = np.where(part == p, w.topk_ids, -1)
+        routed = (part == p).any(axis=1)
+        want[~routed] = -1
+        assert np.array_equal(gids[p], want)
+    rng = np.random.default_rng(5)
+    for t in rng.choice(w.T, 64, replace=False):
+        q, sf = oracle.quant_nvfp4_row(w.x[t], w.global_scale)
+        for p in set(part[t][part[t] >= 0].tolist()):
+            assert np.array_equal(rx[p, t].cpu().numpy(), q) and np.array_equal(rsf[p, t].cpu().numpy(), sf)
+    assert int(st.item()) == 0
