@@ -77,6 +77,9 @@ def _load():
             "oracle_combine": (None, [ctypes.c_int, P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, P, P, P, P, P]),
             "oracle_dispatch_layout": (None, [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P]),
+            "oracle_route_meta_aligned": (ctypes.c_int, [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                         ctypes.c_int, ctypes.c_int, P, P, P, P, P]),
+            "oracle_quant_fp8_g128_ue8m0_row": (None, [P, ctypes.c_int, P, P]),
             "oracle_dispatch_partitioned": (None, [ctypes.c_int, P, i64, i64, ctypes.c_int, P, P, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int32, f32, P, P, P, P]),
             "oracle_combine_partitioned": (None, [P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
@@ -287,3 +290,33 @@ def combine_partitioned(partial: np.ndarray, topk_ids: np.ndarray, E: int, P: in
     out = np.empty((T, H), np.uint16)
     _load().oracle_combine_partitioned(_ptr(pa), T, S, H, _ptr(ids), K, E, P, _ptr(out))
     return out
+
+
+# ---------------------------------------------------------------------------
+# DeepGEMM consumer formats: expert alignment, UE8M0 scales
+# ---------------------------------------------------------------------------
+
+def route_meta_aligned(topk_ids: np.ndarray, E: int, A: int, P: int = 1, M: int = 0) -> Meta:
+    """Metadata with every expert segment starting at a multiple of A; reorder_topk_ids holds
+    seg_indptr[E] entries, -1 on padding rows."""
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    T, K = ids.shape
+    seg = np.zeros(E + 1, np.int64)
+    s2d = np.empty(T * K, np.int32)
+    reo = np.empty(max(T * K + E * (A - 1), 1), np.int32)
+    mm = np.zeros(E, np.int32)
+    pc = np.zeros(max(P, 1), np.int32)
+    st = _load().oracle_route_meta_aligned(_ptr(ids), T, K, E, P, M, A, _ptr(seg), _ptr(s2d), _ptr(reo),
+                                           _ptr(mm), _ptr(pc))
+    n = int(seg[-1])
+    return Meta(seg, s2d, reo[:n].copy(), mm, pc[:P], expected_m(T, K, E) if E else 0, int(st))
+
+
+def quant_fp8_ue8m0_row(x_row: np.ndarray):
+    """(codes [H] uint8, UE8M0 scale bytes [H/128] uint8)."""
+    x_row = np.ascontiguousarray(x_row, dtype=np.uint16)
+    H = x_row.shape[0]
+    q = np.empty(H, np.uint8)
+    e = np.empty(H // 128, np.uint8)
+    _load().oracle_quant_fp8_g128_ue8m0_row(_ptr(x_row), H, _ptr(q), _ptr(e))
+    return q, e

@@ -529,3 +529,94 @@ void oracle_combine_partitioned(const uint16_t *partial, int64_t T, int64_t num_
     }
     free(acc);
 }
+
+/* ------------------------------------------------------------------------- */
+/* consumer formats for DeepGEMM (f3)                                          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Routing metadata with expert_alignment A (buffer.dispatch(..., expert_alignment=128 if
+ * DeepGEMM), _DeepEPDispatcherImplNormal._dispatch_core, "sglang token_dispatcher/deepep.py"
+ * page). Reading: every expert's segment of the contiguous layout starts at a multiple of A:
+ *   seg_indptr[e+1] = seg_indptr[e] + roundup(count[e], A)
+ *   src2dst[i]      = seg_indptr[id_i] + #{j < i valid : id_j = id_i}
+ *   reorder_topk_ids[r] = expert of row r, or -1 for the padding rows of a segment
+ *                          (seg_indptr[E] entries; capacity T*K + E*(A-1))
+ *   masked_m[e] = count[e] (or min(count[e], M)), partition_counts[p] = valid pairs in p.
+ * A = 1 gives oracle_route_meta's result.
+ */
+int oracle_route_meta_aligned(const int32_t *topk_ids, int64_t T, int K, int E, int P, int M, int A,
+                              int64_t *seg_indptr, int32_t *src2dst, int32_t *reorder_topk_ids,
+                              int32_t *masked_m, int32_t *partition_counts)
+{
+    int status = 0;
+    int64_t n_pairs = T * (int64_t)K;
+    int64_t *count = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    int64_t *cursor = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    for (int64_t i = 0; i < n_pairs; i++) {
+        int32_t e = topk_ids[i];
+        if (e >= 0 && e < E) count[e]++;
+        else if (e != -1) status |= ORACLE_BAD_ID;
+    }
+    seg_indptr[0] = 0;
+    for (int e = 0; e < E; e++) seg_indptr[e + 1] = seg_indptr[e] + (count[e] + A - 1) / A * A;
+    for (int64_t r = 0; r < seg_indptr[E]; r++) reorder_topk_ids[r] = -1;
+    for (int e = 0; e < E; e++) cursor[e] = seg_indptr[e];
+    for (int64_t i = 0; i < n_pairs; i++) {
+        int32_t e = topk_ids[i];
+        if (e >= 0 && e < E) {
+            src2dst[i] = (int32_t)cursor[e];
+            reorder_topk_ids[cursor[e]] = e;
+            cursor[e]++;
+        } else {
+            src2dst[i] = -1;
+        }
+    }
+    for (int e = 0; e < E; e++) {
+        int64_t c = count[e];
+        if (M > 0 && c > M) {
+            status |= ORACLE_CAPACITY;
+            c = M;
+        }
+        if (masked_m) masked_m[e] = (int32_t)c;
+    }
+    if (partition_counts && P > 0) {
+        int ep = E / P;
+        for (int p = 0; p < P; p++) {
+            int64_t c = 0;
+            for (int e = p * ep; e < (p + 1) * ep; e++) c += count[e];
+            partition_counts[p] = (int32_t)c;
+        }
+    }
+    free(count);
+    free(cursor);
+    return status;
+}
+
+/*
+ * FP8 group-128 quantisation with power-of-two UE8M0 scales (round_scale / use_ue8m0 of
+ * low_latency_dispatch and scale_ue8m0 of sglang_per_token_group_quant_fp8, deepep.py page).
+ * Reading: s = max(amax, 1e-10) / 448 as in oracle_quant_fp8_g128_row, rounded UP to a
+ * power of two s2 = 2^ceil(log2 s) (so |x / s2| <= 448); q = E4M3(x / s2); the stored
+ * scale is the UE8M0 byte log2(s2) + 127. Four consecutive groups' bytes form one
+ * little-endian int32 ("int32-packed").
+ */
+void oracle_quant_fp8_g128_ue8m0_row(const uint16_t *x, int H, uint8_t *q, uint8_t *scale_exp)
+{
+    for (int g = 0; g < H / 128; g++) {
+        const uint16_t *xg = x + (size_t)g * 128;
+        float amax = 0.0f;
+        for (int j = 0; j < 128; j++) {
+            float v = fabsf(bf16_to_float(xg[j]));
+            if (v > amax) amax = v;
+        }
+        float a = amax > 1e-10f ? amax : 1e-10f;
+        float s = a / 448.0f;
+        int ex;
+        double m = frexp((double)s, &ex);            /* s = m * 2^ex, m in [0.5, 1) */
+        int k = (m == 0.5) ? ex - 1 : ex;             /* smallest k with 2^k >= s */
+        float s2 = (float)ldexp(1.0, k);
+        for (int j = 0; j < 128; j++) q[(size_t)g * 128 + j] = oracle_e4m3_from_float(bf16_to_float(xg[j]) / s2);
+        scale_exp[g] = (uint8_t)(k + 127);
+    }
+}

@@ -1,0 +1,64 @@
+"""Pins for the oracle's DeepGEMM consumer formats (CPU only): expert-aligned metadata and
+FP8 group-128 quantisation with power-of-two UE8M0 scales.
+
+Aligned metadata is checked against the unaligned metadata (pinned separately) through
+the closed-form shift of every segment, against bincount, and by brute force; UE8M0 scales
+against exact rational bounds (2^(b-128) < amax/448 <= 2^(b-127), amax/448 taken in binary32
+as the definition states) and the codes against torch's float8_e4m3fn cast of the exactly
+scaled values.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import bf16_bits_to_f32, f32_to_bf16_bits, make_case
+
+
+@pytest.mark.parametrize("A", [1, 2, 8, 128])
+@pytest.mark.parametrize("seed", range(4))
+def test_aligned_metadata_is_the_unaligned_one_shifted(A, seed):
+    w = make_case(200, 16, 24, 6, seed=seed, routing="replace", invalid_rate=0.1)
+    u = oracle.route_meta(w.topk_ids, w.E, P=4)
+    a = oracle.route_meta_aligned(w.topk_ids, w.E, A, P=4)
+    flat = w.topk_ids.reshape(-1)
+    cnt = np.bincount(flat[flat >= 0], minlength=w.E)
+    assert a.seg_indptr.tolist() == [0] + np.cumsum((cnt + A - 1) // A * A).tolist()
+    assert (a.seg_indptr % A == 0).all()
+    v = flat >= 0
+    shift = a.seg_indptr[flat[v]] - u.seg_indptr[flat[v]]
+    assert np.array_equal(a.src2dst[v], u.src2dst[v] + shift)
+    assert (a.src2dst[~v] == -1).all()
+    assert np.array_equal(a.masked_m, u.masked_m) and np.array_equal(a.partition_counts, u.partition_counts)
+    # reorder: the expert of every real row, -1 on every padding row
+    want = np.full(int(a.seg_indptr[-1]), -1)
+    want[a.src2dst[v]] = flat[v]
+    assert np.array_equal(a.reorder_topk_ids, want)
+    if A == 1:
+        assert np.array_equal(a.seg_indptr, u.seg_indptr) and np.array_equal(a.src2dst, u.src2dst)
+
+
+def test_ue8m0_scales_and_codes():
+    w = make_case(6, 1024, 4, 1, seed=41, std=3.0, zero_tokens=1)
+    for t in range(w.T):
+        q, b = oracle.quant_fp8_ue8m0_row(w.x[t])
+        x = bf16_bits_to_f32(w.x[t]).reshape(-1, 128)
+        for g in range(x.shape[0]):
+            amax = float(np.abs(x[g]).max())
+            s = Fraction(float(np.float32(max(amax, np.float32(1e-10))) / np.float32(448.0)))
+            k = int(b[g]) - 127
+            assert Fraction(2) ** (k - 1) < s <= Fraction(2) ** k          # the power of two just above
+            scaled = (x[g].astype(np.float64) * 2.0 ** (-k)).astype(np.float32)  # exact: power-of-two scaling
+            assert np.all(np.abs(scaled) <= 448)
+            ref = torch.from_numpy(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(q[g * 128:(g + 1) * 128], ref)
+
+
+def test_ue8m0_constant_group_uses_powers_of_two():
+    row = f32_to_bf16_bits(np.concatenate([np.full(128, 448.0), np.full(128, 1.0)]).astype(np.float32))
+    q, b = oracle.quant_fp8_ue8m0_row(row)
+    assert b.tolist() == [127, 127 - 8]                 # 448/448 = 2^0; 1/448 -> 2^-8
+    assert (q[:128] == 0x7E).all()                       # 448 / 1 = 448
+    assert (q[128:] == 0x78).all()                       # 1 / 2^-8 = 256 = 2^8 -> e4m3 0x78
