@@ -31,7 +31,7 @@ BAD_ID = 1
 CAPACITY = 2
 
 MODES = {"normal": 0, "masked": 1}
-QUANTS = {"none": 0, "fp8g128": 1, "nvfp4b16": 2}
+QUANTS = {"none": 0, "fp8g128": 1, "nvfp4b16": 2, "fp8_passthrough": 4}
 
 _lock = threading.Lock()
 _lib = None
@@ -202,6 +202,8 @@ def out_shapes(mode: str, quant: str, T: int, H: int, K: int, E: int, M: int, ro
     lead = (rows if rows is not None else T * K,) if mode == "normal" else (E, M)
     if quant == "none":
         return lead + (H,), np.uint16, None, None
+    if quant == "fp8_passthrough":
+        return lead + (H,), np.uint8, None, None
     if quant == "fp8g128":
         return lead + (H,), np.uint8, lead + (H // 128,), np.float32
     return lead + (H // 2,), np.uint8, lead + (H // 16,), np.uint8
@@ -215,8 +217,9 @@ def _filled(shape, dtype, fill: int) -> np.ndarray:
 
 def dispatch(mode: str, quant: str, x: np.ndarray, topk_ids: np.ndarray, meta: Meta, E: int,
              M: int = 0, global_scale: float = 0.0, rows: Optional[int] = None, fill: int = 0):
-    """Returns (q, scales) in the layout of ``mode``; untouched bytes hold ``fill``."""
-    x = np.ascontiguousarray(x, dtype=np.uint16)
+    """Returns (q, scales) in the layout of ``mode``; untouched bytes hold ``fill``.
+    For quant "fp8_passthrough" x is [T, H] uint8 codes."""
+    x = np.ascontiguousarray(x, dtype=np.uint8 if quant == "fp8_passthrough" else np.uint16)
     ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
     T, H = x.shape
     K = ids.shape[1]

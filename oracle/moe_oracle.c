@@ -356,7 +356,10 @@ static int64_t dest_row(int mode, int64_t i, const int32_t *topk_ids, int E, int
  * rank = src2dst[i] - seg_indptr[e] of expert e (the same stable order as normal
  * mode), slots >= M are dropped. quant: 0 none (bf16 rows), 1 FP8 g128
  * (q rows of H bytes + fp32 scales [.., H/128]), 2 NVFP4 b16 (q rows of H/2 bytes +
- * e4m3 scales [.., H/16]). Each destination quantises its token afresh.
+ * e4m3 scales [.., H/16]), 4 rows that already hold one-byte codes (per-tensor FP8: the
+ * diff page's _deepep_permute allocates gateup_input with fp8_dtype when use_fp8_w8a8 and
+ * not use_block_quant) copied as H bytes; x is then read as [T, H] bytes. Each destination
+ * quantises its token afresh.
  */
 void oracle_dispatch(int mode, int quant, const uint16_t *x, int64_t T, int H,
                      const int32_t *topk_ids, int K, int E, int M,
@@ -368,7 +371,9 @@ void oracle_dispatch(int mode, int quant, const uint16_t *x, int64_t T, int H,
         for (int k = 0; k < K; k++) {
             int64_t r = dest_row(mode, t * K + k, topk_ids, E, M, src2dst, seg_indptr);
             if (r < 0) continue;
-            if (quant == 0) {
+            if (quant == 4) {
+                memcpy((uint8_t *)out_q + (size_t)r * H, (const uint8_t *)x + (size_t)t * H, (size_t)H);
+            } else if (quant == 0) {
                 memcpy((uint16_t *)out_q + (size_t)r * H, row, (size_t)H * 2);
             } else if (quant == 1) {
                 oracle_quant_fp8_g128_row(row, H, (uint8_t *)out_q + (size_t)r * H,

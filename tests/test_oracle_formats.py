@@ -62,3 +62,24 @@ def test_ue8m0_constant_group_uses_powers_of_two():
     assert b.tolist() == [127, 127 - 8]                 # 448/448 = 2^0; 1/448 -> 2^-8
     assert (q[:128] == 0x7E).all()                       # 448 / 1 = 448
     assert (q[128:] == 0x78).all()                       # 1 / 2^-8 = 256 = 2^8 -> e4m3 0x78
+
+
+@pytest.mark.parametrize("mode", ["normal", "masked"])
+def test_fp8_passthrough_rows_are_byte_copies(mode):
+    """Per-tensor FP8 rows (already one-byte codes) are copied unchanged to their destinations."""
+    w = make_case(30, 96, 6, 3, seed=61, invalid_rate=0.1)
+    codes = np.random.default_rng(62).integers(0, 256, size=(w.T, w.H), dtype=np.uint8)
+    M = 40 if mode == "masked" else 0
+    m = oracle.route_meta(w.topk_ids, w.E, M=M)
+    q, s = oracle.dispatch(mode, "fp8_passthrough", codes, w.topk_ids, m, w.E, M=M, fill=0xC3)
+    assert s is None
+    rows = q.reshape(-1, w.H)
+    flat = w.topk_ids.reshape(-1)
+    hit = np.zeros(rows.shape[0], bool)
+    for i, d in enumerate(m.src2dst):
+        if d < 0:
+            continue
+        r = d if mode == "normal" else flat[i] * M + d - m.seg_indptr[flat[i]]
+        assert np.array_equal(rows[r], codes[i // w.K])
+        hit[r] = True
+    assert (rows[~hit] == 0xC3).all()
