@@ -42,7 +42,13 @@ MODES = {"normal": MOE_MODE_NORMAL, "masked": MOE_MODE_MASKED}
 MOE_QUANT_NONE = 0
 MOE_QUANT_FP8_G128 = 1
 MOE_QUANT_NVFP4_B16 = 2
-QUANTS = {"none": MOE_QUANT_NONE, "fp8g128": MOE_QUANT_FP8_G128, "nvfp4b16": MOE_QUANT_NVFP4_B16}
+MOE_QUANT_FP8_G128_UE8M0 = 3
+QUANTS = {"none": MOE_QUANT_NONE, "fp8g128": MOE_QUANT_FP8_G128, "nvfp4b16": MOE_QUANT_NVFP4_B16,
+          "fp8g128_ue8m0": MOE_QUANT_FP8_G128_UE8M0, "fp8_passthrough": 4}
+MOE_QUANT_FP8_PASSTHROUGH = 4
+MOE_SCALES_ROW_MAJOR = 0
+MOE_SCALES_COL_MAJOR = 1
+SCALE_LAYOUTS = {"row": MOE_SCALES_ROW_MAJOR, "col": MOE_SCALES_COL_MAJOR}
 
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_TOPK = 16
@@ -62,6 +68,11 @@ _SIGNATURES = {
     "moe_route_dispatch": (_int, [_int, _int, _P, _i64, _int, _P, _int, _int, _int, _int, _f32, _P, _P, _P, _P,
                                   _P, _P, _P, _sz, _P, _P, _P, _P]),
     "moe_dispatch_layout": (_int, [_P, _i64, _int, _int, _int, _P, _P, _P, _P, _P]),
+    "moe_route_meta_ex": (_int, [_P, _int, _i64, _int, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 _sz, _P, _P]),
+    "moe_dispatch_ex": (_int, [_int, _int, _int, _P, _i64, _int, _P, _int, _int, _int, _i64, _P, _P, _f32, _P, _P,
+                               _P, _P]),
+    "moe_combine_ex": (_int, [_int, _P, _i64, _int, _int, _int, _int, _i64, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch_partitioned": (_int, [_int, _P, _i64, _i64, _int, _P, _P, _int, _int, _int, _i32, _f32, _P, _P,
                                         _P, _P, _P, _P]),
     "moe_combine_partitioned": (_int, [_P, _i64, _i64, _int, _P, _int, _int, _int, _P, _P, _P]),
@@ -220,6 +231,51 @@ def moe_convert_probe(x: torch.Tensor, e4m3: Optional[torch.Tensor] = None, e2m1
     _check(st, "moe_convert_probe")
 
 
+def moe_route_meta_ex(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torch.Tensor, src2dst: torch.Tensor,
+                      reorder_topk_ids: torch.Tensor, masked_m: torch.Tensor, dev_status: torch.Tensor,
+                      workspace: Optional[torch.Tensor] = None, num_partitions: int = 1,
+                      max_tokens_per_expert: int = 0, expert_alignment: int = 1,
+                      partition_counts: Optional[torch.Tensor] = None,
+                      topk_ids_i32_out: Optional[torch.Tensor] = None, stream=None) -> int:
+    """moe_route_meta with expert segments aligned to ``expert_alignment`` rows and int32 or int64
+    ``topk_ids`` (optionally also written as int32 to ``topk_ids_i32_out``); returns expected_m."""
+    T, K = topk_ids.shape
+    em = ctypes.c_int32(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load_library().moe_route_meta_ex(_ptr(topk_ids), topk_ids.element_size(), T, K, num_experts,
+                                          num_partitions, max_tokens_per_expert, expert_alignment, _ptr(seg_indptr),
+                                          _ptr(src2dst), _ptr(reorder_topk_ids), _ptr(masked_m),
+                                          _ptr(partition_counts), _ptr(topk_ids_i32_out), ctypes.byref(em),
+                                          _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _check(st, "moe_route_meta_ex")
+    return int(em.value)
+
+
+def moe_dispatch_ex(mode: str, quant: str, scale_layout: str, hidden_states: torch.Tensor, topk_ids: torch.Tensor,
+                    num_experts: int, src2dst: torch.Tensor, seg_indptr: torch.Tensor, out_q: torch.Tensor,
+                    out_scales: Optional[torch.Tensor], dev_status: torch.Tensor, max_tokens_per_expert: int = 0,
+                    out_rows: int = 0, input_global_scale: float = 0.0, stream=None) -> None:
+    T, H = hidden_states.shape
+    K = topk_ids.shape[1]
+    st = load_library().moe_dispatch_ex(MODES[mode], QUANTS[quant], SCALE_LAYOUTS[scale_layout], _ptr(hidden_states),
+                                        T, H, _ptr(topk_ids), K, num_experts, max_tokens_per_expert, int(out_rows),
+                                        _ptr(src2dst), _ptr(seg_indptr), float(input_global_scale), _ptr(out_q),
+                                        _ptr(out_scales), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_dispatch_ex")
+
+
+def moe_combine_ex(mode: str, expert_out: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                   num_experts: int, src2dst: torch.Tensor, seg_indptr: torch.Tensor, out: torch.Tensor,
+                   dev_status: torch.Tensor, max_tokens_per_expert: int = 0, expert_out_rows: int = 0,
+                   stream=None) -> None:
+    T, K = topk_ids.shape
+    H = out.shape[1]
+    st = load_library().moe_combine_ex(MODES[mode], _ptr(expert_out), T, H, K, num_experts, max_tokens_per_expert,
+                                       int(expert_out_rows), _ptr(topk_ids), _ptr(src2dst), _ptr(seg_indptr),
+                                       _ptr(topk_weights), _ptr(out), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_combine_ex")
+
+
 def moe_dispatch_layout(topk_ids: torch.Tensor, num_experts: int, num_partitions: int,
                         num_tokens_per_rank: torch.Tensor, is_token_in_rank: torch.Tensor, dev_status: torch.Tensor,
                         num_tokens_per_expert: Optional[torch.Tensor] = None, stream=None) -> None:
@@ -313,6 +369,10 @@ def dispatch_out_shapes(mode: str, quant: str, T: int, H: int, K: int, E: int, M
         return lead + (H,), torch.bfloat16, None, None
     if quant == "fp8g128":
         return lead + (H,), torch.uint8, lead + (H // 128,), torch.float32
+    if quant == "fp8g128_ue8m0":
+        return lead + (H,), torch.uint8, lead + (H // 128,), torch.uint8
+    if quant == "fp8_passthrough":
+        return lead + (H,), torch.uint8, None, None
     return lead + (H // 2,), torch.uint8, lead + (H // 16,), torch.uint8
 
 

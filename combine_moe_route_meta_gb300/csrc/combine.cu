@@ -176,7 +176,8 @@ cudaError_t launch_variant(const LaunchCtx& ctx, const CombineArgs& a) {
 cudaError_t launch_combine(const LaunchCtx& ctx, int mode, const uint16_t* expert_out, int64_t T,
                            int H, int K, int E, int M, const int32_t* topk_ids,
                            const int32_t* src2dst, const int64_t* seg_indptr,
-                           const float* topk_weights, uint16_t* out, int32_t* dev_status) {
+                           const float* topk_weights, uint16_t* out, int32_t* dev_status,
+                           int64_t expert_out_rows) {
     CombineArgs a{};
     a.eo = expert_out;
     a.T = T;
@@ -192,7 +193,7 @@ cudaError_t launch_combine(const LaunchCtx& ctx, int mode, const uint16_t* exper
     a.status = dev_status;
     a.units_per_row = (H + kSlice - 1) / kSlice;
     a.n_units = T * a.units_per_row;
-    a.max_row = T * K;
+    a.max_row = expert_out_rows > 0 ? expert_out_rows : T * K;
     return mode == MOE_MODE_MASKED ? launch_variant<true>(ctx, a) : launch_variant<false>(ctx, a);
 }
 

@@ -53,7 +53,8 @@ struct DispatchArgs {
     int32_t* status;
     int units_per_row;
     int64_t n_units;
-    int64_t max_row;  // exclusive bound on normal-mode rows (T*K)
+    int64_t max_row;  // exclusive bound on normal-mode rows (the output's row capacity)
+    ScaleLayout L;
 };
 
 // destination row of pair t*K + lane (lanes >= K return -1); s_seg: seg_indptr in smem
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 
     while (u < a.n_units) {
         const int64_t my_row = dest_row<MASKED>(a, s_seg, t, lane);
-        quantise_store<QUANT>(sl, active, lane, col, H, a.K, my_row, a.g, a.out_q, a.out_s);
+        quantise_store<QUANT>(sl, active, lane, col, H, a.K, my_row, a.g, a.out_q, a.out_s, a.L);
         u += nwarps;
         if (u >= a.n_units) break;
         t = u / a.units_per_row;
@@ -166,7 +167,8 @@ cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t 
 cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uint16_t* x, int64_t T,
                             int H, const int32_t* topk_ids, int K, int E, int M,
                             const int32_t* src2dst, const int64_t* seg_indptr, float global_scale,
-                            void* out_q, void* out_scales, int32_t* dev_status) {
+                            void* out_q, void* out_scales, int32_t* dev_status, int scale_layout,
+                            int64_t out_rows) {
     DispatchArgs a{};
     a.x = x;
     a.T = T;
@@ -183,8 +185,11 @@ cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uin
     a.status = dev_status;
     a.units_per_row = (H + kSlice - 1) / kSlice;
     a.n_units = T * a.units_per_row;
-    a.max_row = T * K;
+    a.max_row = out_rows > 0 ? out_rows : T * K;
     const bool masked = mode == MOE_MODE_MASKED;
+    a.L.col_major = scale_layout;
+    a.L.M = masked ? M : 0;
+    a.L.rows_al = ((masked ? int64_t(M) : a.max_row) + 3) / 4 * 4;
     switch (quant) {
         case MOE_QUANT_NONE:
             return masked ? launch_variant<MOE_QUANT_NONE, true>(ctx, a)
@@ -192,6 +197,9 @@ cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uin
         case MOE_QUANT_FP8_G128:
             return masked ? launch_variant<MOE_QUANT_FP8_G128, true>(ctx, a)
                           : launch_variant<MOE_QUANT_FP8_G128, false>(ctx, a);
+        case MOE_QUANT_FP8_G128_UE8M0:
+            return masked ? launch_variant<MOE_QUANT_FP8_G128_UE8M0, true>(ctx, a)
+                          : launch_variant<MOE_QUANT_FP8_G128_UE8M0, false>(ctx, a);
         default:
             return masked ? launch_variant<MOE_QUANT_NVFP4_B16, true>(ctx, a)
                           : launch_variant<MOE_QUANT_NVFP4_B16, false>(ctx, a);

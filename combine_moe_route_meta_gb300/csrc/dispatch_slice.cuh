@@ -2,7 +2,8 @@
 // the K destination rows (shared by the dispatch kernels).
 //
 // Q = identity, FP8 e4m3 per 128-element group (sglang_per_token_group_quant_fp8 in
-// _DeepEPDispatcherImplNormal.dispatch_a, "sglang token_dispatcher/deepep.py" page), or
+// _DeepEPDispatcherImplNormal.dispatch_a, "sglang token_dispatcher/deepep.py" page; with
+// round_scale / use_ue8m0 the scale is rounded up to a power of two, kept as a UE8M0 byte), or
 // NVFP4 e2m1 with an e4m3 scale per 16-element block (fp4_quantize in
 // FlashinferDispatcher.dispatch, "sglang token_dispatcher/flashinfer.py" page):
 //   fp8:   s = max(amax, 1e-10) / 448,           q = e4m3(x / s)
@@ -15,6 +16,27 @@
 #include "moe_device.cuh"
 
 namespace moe {
+
+// Where the scales of a destination row go (MOE_SCALES_ROW_MAJOR / MOE_SCALES_COL_MAJOR).
+struct ScaleLayout {
+    int col_major;    // 0: [rows, G] row-major; 1: MN-major with rows padded to a multiple of 4
+    int64_t rows_al;  // column-major: padded rows (normal layout) or padded slots M (masked)
+    int M;            // masked layout: slots per expert; 0 for the contiguous layout
+};
+
+// Element index of group g's scale for destination `row`: fp32 elements, or bytes when
+// `packed4` (UE8M0: four groups per int32 word, little-endian).
+__device__ __forceinline__ int64_t scale_index(const ScaleLayout& L, int64_t row, int g, int G, bool packed4) {
+    if (!L.col_major) return row * G + g;
+    int64_t e = 0, r = row;
+    if (L.M > 0) {
+        e = row / L.M;
+        r = row - e * L.M;
+    }
+    if (!packed4) return (e * G + g) * L.rows_al + r;
+    const int G4 = (G + 3) / 4;
+    return ((e * G4 + g / 4) * L.rows_al + r) * 4 + (g & 3);
+}
 
 // One lane's payload: 16 bf16 elements (two 16-byte vectors) of a token row.
 struct LaneSlice {
@@ -35,7 +57,7 @@ __device__ __forceinline__ LaneSlice load_slice(const uint16_t* src) {
 template <int QUANT>
 __device__ __forceinline__ void quantise_store(const LaneSlice& s, bool active, int lane, int col, int H,
                                                int K, int64_t my_row, float g, void* out_q,
-                                               void* out_s) {
+                                               void* out_s, const ScaleLayout& L = ScaleLayout{0, 0, 0}) {
     if constexpr (QUANT == MOE_QUANT_NONE) {
         uint16_t* out = static_cast<uint16_t*>(out_q);
         for (int k = 0; k < K; k++) {
@@ -73,7 +95,41 @@ __device__ __forceinline__ void quantise_store(const LaneSlice& s, bool active, 
             const int64_t row = __shfl_sync(kFullMask, my_row, k);
             if (row >= 0 && active) {
                 st_v4(out + row * H + col, q);
-                if ((lane & 7) == 0) scales[row * groups + col / 128] = sc;
+                if ((lane & 7) == 0) scales[scale_index(L, row, col / 128, groups, false)] = sc;
+            }
+        }
+    } else if constexpr (QUANT == MOE_QUANT_FP8_G128_UE8M0) {
+        // as FP8 g128, with the scale rounded up to a power of two 2^(ex-127): dividing by it
+        // is exact, so x * 2^(127-ex) gives the same binary32 value as x / 2^(ex-127)
+        float f[16];
+        unpack8(s.v0, f);
+        unpack8(s.v1, f + 8);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+        const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+        const uint32_t bits = __float_as_uint(sc);
+        const uint32_t ex = (bits >> 23) + ((bits & 0x7fffffu) ? 1u : 0u);
+        const float inv = __uint_as_float((254u - ex) << 23);
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; p++) {
+            const uint32_t lo = e4m3x2(__fmul_rn(f[4 * p], inv), __fmul_rn(f[4 * p + 1], inv));
+            const uint32_t hi = e4m3x2(__fmul_rn(f[4 * p + 2], inv), __fmul_rn(f[4 * p + 3], inv));
+            w[p] = lo | (hi << 16);
+        }
+        const uint4 q = make_uint4(w[0], w[1], w[2], w[3]);
+        uint8_t* out = static_cast<uint8_t*>(out_q);
+        uint8_t* sfo = static_cast<uint8_t*>(out_s);
+        const int groups = H / 128;
+        for (int k = 0; k < K; k++) {
+            const int64_t row = __shfl_sync(kFullMask, my_row, k);
+            if (row >= 0 && active) {
+                st_v4(out + row * H + col, q);
+                if ((lane & 7) == 0) sfo[scale_index(L, row, col / 128, groups, true)] = uint8_t(ex);
             }
         }
     } else {  // MOE_QUANT_NVFP4_B16

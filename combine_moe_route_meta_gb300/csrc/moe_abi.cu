@@ -60,21 +60,27 @@ size_t moe_route_meta_workspace_size(int64_t num_tokens, int topk, int num_exper
     return moe::plan_route_meta(num_tokens * topk, num_experts).ws_bytes;
 }
 
-moe_status_t moe_route_meta(const int32_t* topk_ids, int64_t num_tokens, int topk, int num_experts,
-                            int num_partitions, int max_tokens_per_expert, int64_t* seg_indptr,
-                            int32_t* src2dst, int32_t* reorder_topk_ids, int32_t* masked_m,
-                            int32_t* partition_counts, int32_t* expected_m_host, void* workspace,
-                            size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+static moe_status_t route_meta_impl(const void* topk_ids, int ids_bytes, int64_t num_tokens, int topk,
+                                    int num_experts, int num_partitions, int max_tokens_per_expert,
+                                    int expert_alignment, int64_t* seg_indptr, int32_t* src2dst,
+                                    int32_t* reorder_topk_ids, int32_t* masked_m, int32_t* partition_counts,
+                                    int32_t* ids_out, int32_t* expected_m_host, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+    if (ids_bytes != 4 && ids_bytes != 8) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(num_tokens, topk, num_experts);
     if (st != MOE_OK) return st;
     if (num_partitions < 1 || num_experts % num_partitions != 0) return MOE_ERR_INVALID_ARG;
     if (max_tokens_per_expert < 0) return MOE_ERR_INVALID_ARG;
-    if (!seg_indptr || !masked_m || !dev_status) return MOE_ERR_INVALID_ARG;
+    if (expert_alignment < 1) return MOE_ERR_INVALID_ARG;
+    if (expert_alignment > 1024) return MOE_ERR_UNSUPPORTED;
     const int64_t n_pairs = num_tokens * topk;
-    if (n_pairs > 0 && (!topk_ids || !src2dst || !reorder_topk_ids)) return MOE_ERR_INVALID_ARG;
-    if (!aligned(seg_indptr, 8) || !aligned(topk_ids, 4) || !aligned(src2dst, 4) ||
+    if (n_pairs + int64_t(num_experts) * (expert_alignment - 1) > int64_t(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+    if (!seg_indptr || !masked_m || !dev_status) return MOE_ERR_INVALID_ARG;
+    if ((n_pairs > 0 || expert_alignment > 1) && !reorder_topk_ids) return MOE_ERR_INVALID_ARG;
+    if (n_pairs > 0 && (!topk_ids || !src2dst)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(seg_indptr, 8) || !aligned(topk_ids, uintptr_t(ids_bytes)) || !aligned(src2dst, 4) ||
         !aligned(reorder_topk_ids, 4) || !aligned(masked_m, 4) || !aligned(partition_counts, 4) ||
-        !aligned(dev_status, 4))
+        !aligned(ids_out, 4) || !aligned(dev_status, 4))
         return MOE_ERR_INVALID_ARG;
     const moe::RoutePlan plan = moe::plan_route_meta(n_pairs, num_experts);
     if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes || !aligned(workspace, 256)))
@@ -83,26 +89,69 @@ moe_status_t moe_route_meta(const int32_t* topk_ids, int64_t num_tokens, int top
     st = make_ctx(stream, &ctx);
     if (st != MOE_OK) return st;
     if (expected_m_host) *expected_m_host = int32_t((n_pairs + num_experts) / num_experts);
-    return from_cuda(moe::launch_route_meta(ctx, plan, topk_ids, n_pairs, topk, num_experts,
-                                            num_partitions, max_tokens_per_expert, seg_indptr,
-                                            src2dst, reorder_topk_ids, masked_m, partition_counts,
-                                            workspace, dev_status));
+    const bool i64 = ids_bytes == 8;
+    return from_cuda(moe::launch_route_meta(
+        ctx, plan, i64 ? nullptr : static_cast<const int32_t*>(topk_ids), n_pairs, topk, num_experts,
+        num_partitions, max_tokens_per_expert, seg_indptr, src2dst, reorder_topk_ids, masked_m, partition_counts,
+        workspace, dev_status, expert_alignment, i64 ? static_cast<const int64_t*>(topk_ids) : nullptr, ids_out));
 }
 
-moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t* hidden_states,
-                          int64_t num_tokens, int hidden, const int32_t* topk_ids, int topk,
-                          int num_experts, int max_tokens_per_expert, const int32_t* src2dst,
-                          const int64_t* seg_indptr, float input_global_scale, void* out_q,
-                          void* out_scales, int32_t* dev_status, moe_stream_t stream) {
+moe_status_t moe_route_meta(const int32_t* topk_ids, int64_t num_tokens, int topk, int num_experts,
+                            int num_partitions, int max_tokens_per_expert, int64_t* seg_indptr,
+                            int32_t* src2dst, int32_t* reorder_topk_ids, int32_t* masked_m,
+                            int32_t* partition_counts, int32_t* expected_m_host, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+    return route_meta_impl(topk_ids, 4, num_tokens, topk, num_experts, num_partitions, max_tokens_per_expert, 1,
+                           seg_indptr, src2dst, reorder_topk_ids, masked_m, partition_counts, nullptr,
+                           expected_m_host, workspace, workspace_bytes, dev_status, stream);
+}
+
+moe_status_t moe_route_meta_ex(const void* topk_ids, int topk_ids_bytes, int64_t num_tokens, int topk,
+                               int num_experts, int num_partitions, int max_tokens_per_expert,
+                               int expert_alignment, int64_t* seg_indptr, int32_t* src2dst,
+                               int32_t* reorder_topk_ids, int32_t* masked_m, int32_t* partition_counts,
+                               int32_t* topk_ids_i32_out, int32_t* expected_m_host, void* workspace,
+                               size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+    return route_meta_impl(topk_ids, topk_ids_bytes, num_tokens, topk, num_experts, num_partitions,
+                           max_tokens_per_expert, expert_alignment, seg_indptr, src2dst, reorder_topk_ids,
+                           masked_m, partition_counts, topk_ids_i32_out, expected_m_host, workspace,
+                           workspace_bytes, dev_status, stream);
+}
+
+static bool valid_quant(moe_quant_t q) {
+    return q == MOE_QUANT_NONE || q == MOE_QUANT_FP8_G128 || q == MOE_QUANT_NVFP4_B16 ||
+           q == MOE_QUANT_FP8_G128_UE8M0 || q == MOE_QUANT_FP8_PASSTHROUGH;
+}
+
+// A pass-through row of H one-byte codes moves exactly like a bf16 row of H/2 elements.
+static void passthrough_as_copy(moe_quant_t* q, int* hidden) {
+    if (*q == MOE_QUANT_FP8_PASSTHROUGH) {
+        *q = MOE_QUANT_NONE;
+        *hidden /= 2;
+    }
+}
+
+static bool is_fp8(moe_quant_t q) { return q == MOE_QUANT_FP8_G128 || q == MOE_QUANT_FP8_G128_UE8M0; }
+
+static moe_status_t dispatch_impl(moe_mode_t mode, moe_quant_t quant, moe_scale_layout_t layout,
+                                  const uint16_t* hidden_states, int64_t num_tokens, int hidden,
+                                  const int32_t* topk_ids, int topk, int num_experts, int max_tokens_per_expert,
+                                  int64_t out_rows, const int32_t* src2dst, const int64_t* seg_indptr,
+                                  float input_global_scale, void* out_q, void* out_scales, int32_t* dev_status,
+                                  moe_stream_t stream) {
     if (mode != MOE_MODE_NORMAL && mode != MOE_MODE_MASKED) return MOE_ERR_INVALID_ARG;
-    if (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_G128 && quant != MOE_QUANT_NVFP4_B16)
-        return MOE_ERR_INVALID_ARG;
+    if (!valid_quant(quant)) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_SCALES_ROW_MAJOR && layout != MOE_SCALES_COL_MAJOR) return MOE_ERR_INVALID_ARG;
+    if (layout == MOE_SCALES_COL_MAJOR && !is_fp8(quant)) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(num_tokens, topk, num_experts);
     if (st != MOE_OK) return st;
     if (hidden <= 0 || hidden % 16 != 0) return MOE_ERR_INVALID_ARG;
-    if (quant == MOE_QUANT_FP8_G128 && hidden % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (is_fp8(quant) && hidden % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (quant == MOE_QUANT_FP8_PASSTHROUGH && hidden % 32 != 0) return MOE_ERR_INVALID_ARG;
+    passthrough_as_copy(&quant, &hidden);
     const bool masked = mode == MOE_MODE_MASKED;
     if (masked && max_tokens_per_expert < 1) return MOE_ERR_INVALID_ARG;
+    if (!masked && out_rows != 0 && out_rows < num_tokens * topk) return MOE_ERR_INVALID_ARG;
     if (!dev_status) return MOE_ERR_INVALID_ARG;
     if (num_tokens == 0) return MOE_OK;
     if (!hidden_states || !src2dst || !out_q) return MOE_ERR_INVALID_ARG;
@@ -118,7 +167,29 @@ moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t* hi
     return from_cuda(moe::launch_dispatch(ctx, int(mode), int(quant), hidden_states, num_tokens,
                                           hidden, topk_ids, topk, num_experts,
                                           masked ? max_tokens_per_expert : 0, src2dst, seg_indptr,
-                                          input_global_scale, out_q, out_scales, dev_status));
+                                          input_global_scale, out_q, out_scales, dev_status, int(layout),
+                                          masked ? 0 : out_rows));
+}
+
+moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t* hidden_states,
+                          int64_t num_tokens, int hidden, const int32_t* topk_ids, int topk,
+                          int num_experts, int max_tokens_per_expert, const int32_t* src2dst,
+                          const int64_t* seg_indptr, float input_global_scale, void* out_q,
+                          void* out_scales, int32_t* dev_status, moe_stream_t stream) {
+    return dispatch_impl(mode, quant, MOE_SCALES_ROW_MAJOR, hidden_states, num_tokens, hidden, topk_ids, topk,
+                         num_experts, max_tokens_per_expert, 0, src2dst, seg_indptr, input_global_scale, out_q,
+                         out_scales, dev_status, stream);
+}
+
+moe_status_t moe_dispatch_ex(moe_mode_t mode, moe_quant_t quant, moe_scale_layout_t scale_layout,
+                             const uint16_t* hidden_states, int64_t num_tokens, int hidden,
+                             const int32_t* topk_ids, int topk, int num_experts, int max_tokens_per_expert,
+                             int64_t out_rows, const int32_t* src2dst, const int64_t* seg_indptr,
+                             float input_global_scale, void* out_q, void* out_scales, int32_t* dev_status,
+                             moe_stream_t stream) {
+    return dispatch_impl(mode, quant, scale_layout, hidden_states, num_tokens, hidden, topk_ids, topk, num_experts,
+                         max_tokens_per_expert, out_rows, src2dst, seg_indptr, input_global_scale, out_q,
+                         out_scales, dev_status, stream);
 }
 
 moe_status_t moe_route_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t* hidden_states,
@@ -129,13 +200,14 @@ moe_status_t moe_route_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16
                                 int32_t* expected_m_host, void* workspace, size_t workspace_bytes,
                                 void* out_q, void* out_scales, int32_t* dev_status, moe_stream_t stream) {
     if (mode != MOE_MODE_NORMAL && mode != MOE_MODE_MASKED) return MOE_ERR_INVALID_ARG;
-    if (quant != MOE_QUANT_NONE && quant != MOE_QUANT_FP8_G128 && quant != MOE_QUANT_NVFP4_B16)
-        return MOE_ERR_INVALID_ARG;
+    if (!valid_quant(quant)) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(num_tokens, topk, num_experts);
     if (st != MOE_OK) return st;
     if (num_partitions < 1 || num_experts % num_partitions != 0) return MOE_ERR_INVALID_ARG;
     if (hidden <= 0 || hidden % 16 != 0) return MOE_ERR_INVALID_ARG;
-    if (quant == MOE_QUANT_FP8_G128 && hidden % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (is_fp8(quant) && hidden % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (quant == MOE_QUANT_FP8_PASSTHROUGH && hidden % 32 != 0) return MOE_ERR_INVALID_ARG;
+    passthrough_as_copy(&quant, &hidden);
     const bool masked = mode == MOE_MODE_MASKED;
     if (masked ? max_tokens_per_expert < 1 : max_tokens_per_expert < 0) return MOE_ERR_INVALID_ARG;
     if (!seg_indptr || !masked_m || !dev_status) return MOE_ERR_INVALID_ARG;
@@ -172,17 +244,18 @@ moe_status_t moe_route_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16
                                           input_global_scale, out_q, out_scales, dev_status));
 }
 
-moe_status_t moe_combine(moe_mode_t mode, const uint16_t* expert_out, int64_t num_tokens, int hidden,
-                         int topk, int num_experts, int max_tokens_per_expert,
-                         const int32_t* topk_ids, const int32_t* src2dst, const int64_t* seg_indptr,
-                         const float* topk_weights, uint16_t* out, int32_t* dev_status,
-                         moe_stream_t stream) {
+static moe_status_t combine_impl(moe_mode_t mode, const uint16_t* expert_out, int64_t num_tokens, int hidden,
+                                 int topk, int num_experts, int max_tokens_per_expert, int64_t expert_out_rows,
+                                 const int32_t* topk_ids, const int32_t* src2dst, const int64_t* seg_indptr,
+                                 const float* topk_weights, uint16_t* out, int32_t* dev_status,
+                                 moe_stream_t stream) {
     if (mode != MOE_MODE_NORMAL && mode != MOE_MODE_MASKED) return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(num_tokens, topk, num_experts);
     if (st != MOE_OK) return st;
     if (hidden <= 0 || hidden % 16 != 0) return MOE_ERR_INVALID_ARG;
     const bool masked = mode == MOE_MODE_MASKED;
     if (masked && max_tokens_per_expert < 1) return MOE_ERR_INVALID_ARG;
+    if (!masked && expert_out_rows != 0 && expert_out_rows < num_tokens * topk) return MOE_ERR_INVALID_ARG;
     if (!dev_status) return MOE_ERR_INVALID_ARG;
     if (num_tokens == 0) return MOE_OK;
     if (!expert_out || !src2dst || !topk_weights || !out) return MOE_ERR_INVALID_ARG;
@@ -196,7 +269,25 @@ moe_status_t moe_combine(moe_mode_t mode, const uint16_t* expert_out, int64_t nu
     if (st != MOE_OK) return st;
     return from_cuda(moe::launch_combine(ctx, int(mode), expert_out, num_tokens, hidden, topk,
                                          num_experts, masked ? max_tokens_per_expert : 0, topk_ids,
-                                         src2dst, seg_indptr, topk_weights, out, dev_status));
+                                         src2dst, seg_indptr, topk_weights, out, dev_status,
+                                         masked ? 0 : expert_out_rows));
+}
+
+moe_status_t moe_combine(moe_mode_t mode, const uint16_t* expert_out, int64_t num_tokens, int hidden,
+                         int topk, int num_experts, int max_tokens_per_expert,
+                         const int32_t* topk_ids, const int32_t* src2dst, const int64_t* seg_indptr,
+                         const float* topk_weights, uint16_t* out, int32_t* dev_status,
+                         moe_stream_t stream) {
+    return combine_impl(mode, expert_out, num_tokens, hidden, topk, num_experts, max_tokens_per_expert, 0,
+                        topk_ids, src2dst, seg_indptr, topk_weights, out, dev_status, stream);
+}
+
+moe_status_t moe_combine_ex(moe_mode_t mode, const uint16_t* expert_out, int64_t num_tokens, int hidden,
+                            int topk, int num_experts, int max_tokens_per_expert, int64_t expert_out_rows,
+                            const int32_t* topk_ids, const int32_t* src2dst, const int64_t* seg_indptr,
+                            const float* topk_weights, uint16_t* out, int32_t* dev_status, moe_stream_t stream) {
+    return combine_impl(mode, expert_out, num_tokens, hidden, topk, num_experts, max_tokens_per_expert,
+                        expert_out_rows, topk_ids, src2dst, seg_indptr, topk_weights, out, dev_status, stream);
 }
 
 moe_status_t moe_dispatch_layout(const int32_t* topk_ids, int64_t num_tokens, int topk, int num_experts,

@@ -92,12 +92,14 @@ RoutePlan plan_route_meta(int64_t n_pairs, int num_experts);
 cudaError_t launch_route_meta(const LaunchCtx& ctx, const RoutePlan& plan, const int32_t* topk_ids,
                               int64_t n_pairs, int K, int E, int P, int M, int64_t* seg_indptr,
                               int32_t* src2dst, int32_t* reorder_topk_ids, int32_t* masked_m,
-                              int32_t* partition_counts, void* workspace, int32_t* dev_status);
+                              int32_t* partition_counts, void* workspace, int32_t* dev_status, int A = 1,
+                              const int64_t* topk_ids64 = nullptr, int32_t* ids_out = nullptr);
 
 cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uint16_t* x, int64_t T,
                             int H, const int32_t* topk_ids, int K, int E, int M,
                             const int32_t* src2dst, const int64_t* seg_indptr, float global_scale,
-                            void* out_q, void* out_scales, int32_t* dev_status);
+                            void* out_q, void* out_scales, int32_t* dev_status, int scale_layout = 0,
+                            int64_t out_rows = 0);
 
 // Fused route + dispatch for small batches (one kernel, one block per token).
 constexpr int64_t kFusedMaxPairs = 4096;
@@ -128,6 +130,7 @@ cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t 
 cudaError_t launch_combine(const LaunchCtx& ctx, int mode, const uint16_t* expert_out, int64_t T,
                            int H, int K, int E, int M, const int32_t* topk_ids,
                            const int32_t* src2dst, const int64_t* seg_indptr,
-                           const float* topk_weights, uint16_t* out, int32_t* dev_status);
+                           const float* topk_weights, uint16_t* out, int32_t* dev_status,
+                           int64_t expert_out_rows = 0);
 
 }  // namespace moe

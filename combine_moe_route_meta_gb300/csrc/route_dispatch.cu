@@ -13,7 +13,8 @@
 //  2. for each of its K pairs (expert e_k, flattened index i_k) it needs only two counts
 //     over all T*K ids: #{valid ids < e_k} = seg_indptr[e_k] and #{j < i_k : id_j = e_k},
 //     the stable rank. All threads take both counts in one strided pass over the ids
-//     (register counters), reduce them with warp shuffles and one shared-memory step;
+//     (register counters), reduce them with the hardware warp reduction and one
+//     shared-memory step;
 //  3. it writes its K entries of src2dst / reorder_topk_ids, and quantises and stores its
 //     row slices into the K destination rows (dispatch_slice.cuh).
 // Block T builds the full histogram and its exclusive scan and writes seg_indptr,
@@ -120,7 +121,7 @@ __device__ void fused_global_metadata(const FusedArgs& a, int* smem) {
     }
 }
 
-template <int QUANT, bool MASKED>
+template <int QUANT, bool MASKED, int KMAX>
 __global__ void route_dispatch_small_kernel(FusedArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     pdl_launch_dependents();  // a programmatic dependent (the combine) may start launching
@@ -130,7 +131,7 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
         return;
     }
     int64_t* s_row = reinterpret_cast<int64_t*>(smem_raw);         // [MOE_MAX_TOPK]
-    int* s_part = reinterpret_cast<int*>(s_row + MOE_MAX_TOPK);     // [warps][2 * MOE_MAX_TOPK]
+    int* s_part = reinterpret_cast<int*>(s_row + MOE_MAX_TOPK);     // [warps][2 * KMAX]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     const int t = blockIdx.x, H = a.H, K = a.K, E = a.E;
@@ -144,9 +145,9 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
 
     // 2. per pair k: less[k] = #{valid ids < e_k}, rank[k] = #{j < i_k : id_j == e_k}
     const int base = t * K;
-    int ek[MOE_MAX_TOPK], less[MOE_MAX_TOPK], rank[MOE_MAX_TOPK];
+    int ek[KMAX], less[KMAX], rank[KMAX];
 #pragma unroll
-    for (int k = 0; k < MOE_MAX_TOPK; k++) {
+    for (int k = 0; k < KMAX; k++) {
         ek[k] = k < K ? __ldg(a.ids + base + k) : -2;
         less[k] = 0;
         rank[k] = 0;
@@ -155,22 +156,19 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
         const int v = __ldg(a.ids + j);
         const bool ok = v >= 0;
 #pragma unroll
-        for (int k = 0; k < MOE_MAX_TOPK; k++) {
+        for (int k = 0; k < KMAX; k++) {
             less[k] += (ok && v < ek[k]) ? 1 : 0;
             rank[k] += (v == ek[k] && j < base + k) ? 1 : 0;
         }
     }
 #pragma unroll
-    for (int k = 0; k < MOE_MAX_TOPK; k++) {
+    for (int k = 0; k < KMAX; k++) {
         if (k < K) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                less[k] += __shfl_xor_sync(kFullMask, less[k], o);
-                rank[k] += __shfl_xor_sync(kFullMask, rank[k], o);
-            }
+            const int l = __reduce_add_sync(kFullMask, less[k]);  // hardware warp reduction
+            const int r = __reduce_add_sync(kFullMask, rank[k]);
             if (lane == 0) {
-                s_part[warp * 2 * MOE_MAX_TOPK + k] = less[k];
-                s_part[warp * 2 * MOE_MAX_TOPK + MOE_MAX_TOPK + k] = rank[k];
+                s_part[warp * 2 * KMAX + k] = l;
+                s_part[warp * 2 * KMAX + KMAX + k] = r;
             }
         }
     }
@@ -183,8 +181,8 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
         if (e >= 0 && e < E) {
             int seg_e = 0, r = 0;
             for (int w = 0; w < nw; w++) {
-                seg_e += s_part[w * 2 * MOE_MAX_TOPK + k];
-                r += s_part[w * 2 * MOE_MAX_TOPK + MOE_MAX_TOPK + k];
+                seg_e += s_part[w * 2 * KMAX + k];
+                r += s_part[w * 2 * KMAX + KMAX + k];
             }
             const int d = seg_e + r;
             a.src2dst[i] = d;
@@ -209,7 +207,9 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
 
 template <int QUANT, bool MASKED>
 cudaError_t launch_fused(const LaunchCtx& ctx, const FusedArgs& a) {
-    auto kern = route_dispatch_small_kernel<QUANT, MASKED>;
+    // K <= 8 (the pages' top-8 routing) gets a specialisation with half the counters
+    auto kern = a.K <= 8 ? route_dispatch_small_kernel<QUANT, MASKED, 8>
+                         : route_dispatch_small_kernel<QUANT, MASKED, MOE_MAX_TOPK>;
     int threads = a.units_per_row * 32;
     threads = threads < 128 ? 128 : (threads > 512 ? 512 : threads);
     const size_t token_smem = sizeof(int64_t) * MOE_MAX_TOPK + sizeof(int) * size_t(threads / 32) * 2 * MOE_MAX_TOPK;
@@ -258,6 +258,9 @@ cudaError_t launch_route_dispatch_small(const LaunchCtx& ctx, int mode, int quan
         case MOE_QUANT_FP8_G128:
             return masked ? launch_fused<MOE_QUANT_FP8_G128, true>(ctx, a)
                           : launch_fused<MOE_QUANT_FP8_G128, false>(ctx, a);
+        case MOE_QUANT_FP8_G128_UE8M0:
+            return masked ? launch_fused<MOE_QUANT_FP8_G128_UE8M0, true>(ctx, a)
+                          : launch_fused<MOE_QUANT_FP8_G128_UE8M0, false>(ctx, a);
         default:
             return masked ? launch_fused<MOE_QUANT_NVFP4_B16, true>(ctx, a)
                           : launch_fused<MOE_QUANT_NVFP4_B16, false>(ctx, a);

@@ -26,6 +26,7 @@
 //    over the experts are seg_indptr (block 0 writes the per-expert outputs); it then
 //    finalises its own pairs. No block ever waits for another, so nothing spins.
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 
 #include "moe_device.cuh"
@@ -69,14 +70,17 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 
 // Final per-expert outputs from the histogram held in shared memory.
 // hist[e] (e < E) -> seg (shared, E+1 ints), seg_indptr, masked_m, partition_counts.
-// With `write` false only the shared seg[] is produced.
-__device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int E, int P, int M,
+// Segments are padded to a multiple of A rows (expert_alignment; A = 1: no padding).
+// With `write` false only the shared seg[] is produced; with `write` the per-expert outputs
+// go to memory, including -1 in reorder_topk_ids for every padding row.
+__device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int E, int P, int M, int A,
                                  int64_t* seg_indptr, int32_t* masked_m, int32_t* partition_counts,
-                                 int32_t* status, bool write = true) {
+                                 int32_t* reorder, int32_t* status, bool write = true) {
     const int e = threadIdx.x;  // E <= 1024 == blockDim
     const int c = e < E ? hist[e] : 0;
+    const int padded = (c + A - 1) / A * A;
     int total;
-    const int excl = block_exclusive_scan(c, warp_sums, &total);
+    const int excl = block_exclusive_scan(padded, warp_sums, &total);
     if (e < E) {
         seg[e] = excl;
         if (write) {
@@ -87,6 +91,7 @@ __device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int 
                 set_status(status, MOE_ERR_CAPACITY);
             }
             masked_m[e] = mm;
+            for (int r = c; r < padded; r++) reorder[excl + r] = -1;
         }
     }
     if (e == 0) {
@@ -96,7 +101,9 @@ __device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int 
     __syncthreads();
     if (write && partition_counts != nullptr && e < P) {
         const int ep = E / P;
-        partition_counts[e] = seg[(e + 1) * ep] - seg[e * ep];
+        int n = 0;
+        for (int x = e * ep; x < (e + 1) * ep; x++) n += hist[x];
+        partition_counts[e] = n;
     }
 }
 
@@ -112,8 +119,18 @@ __device__ __forceinline__ int er_rank(int p) { return p >> 11; }
 
 // Phase 1 of every block: per-warp stable ranks and per-warp counters.
 // cnt: shared [32][S]. Fills er[r] (packed expert, rank) for the R rounds of this thread.
+// Expert id of pair i as int32. int64 ids outside the int32 range map to INT32_MIN / INT32_MAX,
+// which are outside [-1, E) and so count as bad ids; ids_out (if set) receives the value.
+__device__ __forceinline__ int read_id(const int32_t* __restrict__ ids, const int64_t* __restrict__ ids64,
+                                       int64_t i) {
+    if (ids64 == nullptr) return __ldg(ids + i);
+    const long long v = __ldg(reinterpret_cast<const long long*>(ids64) + i);
+    return v < INT32_MIN ? INT32_MIN : (v > INT32_MAX ? INT32_MAX : int(v));
+}
+
 template <int RMAX>
-__device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, int64_t n_pairs, int E,
+__device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, const int64_t* __restrict__ ids64,
+                                           int32_t* ids_out, int64_t n_pairs, int E,
                                            int R, int64_t warp_base, int* cnt, int (&er)[RMAX],
                                            int32_t* status) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -127,7 +144,8 @@ __device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, int6
             const int64_t i = warp_base + r * 32 + lane;
             int e = -1;
             if (i < n_pairs) {
-                e = __ldg(ids + i);
+                e = read_id(ids, ids64, i);
+                if (ids_out != nullptr) ids_out[i] = e;
                 if (e < -1 || e >= E) {
                     bad = true;
                     e = -1;
@@ -166,9 +184,12 @@ __device__ __forceinline__ void scan_warps(int* cnt, int* hist, int E) {
 }
 
 struct RouteArgs {
-    const int32_t* ids;
+    const int32_t* ids;    // int32 ids, or
+    const int64_t* ids64;  // int64 ids (exactly one of the two is set)
+    int32_t* ids_out;      // optional int32 copy of the ids
     int64_t n_pairs;
     int E, P, M, R;
+    int A;  // expert alignment of the segments (1 = none)
     int64_t* seg_indptr;
     int32_t* src2dst;
     int32_t* reorder;
@@ -201,12 +222,12 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_single_kernel(Rou
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t warp_base = int64_t(w) * 32 * a.R;
     int er[RMAX];
-    warp_ranks<RMAX>(a.ids, a.n_pairs, E, a.R, warp_base, cnt, er, a.status);
+    warp_ranks<RMAX>(a.ids, a.ids64, a.ids_out, a.n_pairs, E, a.R, warp_base, cnt, er, a.status);
     __syncthreads();
     scan_warps(cnt, hist, E);
     __syncthreads();
-    finish_histogram(hist, seg, warp_sums, E, a.P, a.M, a.seg_indptr, a.masked_m,
-                     a.partition_counts, a.status);
+    finish_histogram(hist, seg, warp_sums, E, a.P, a.M, a.A, a.seg_indptr, a.masked_m,
+                     a.partition_counts, a.reorder, a.status);
     // finish_histogram ends with __syncthreads: seg[] and the warp offsets in cnt are final
 #pragma unroll
     for (int r = 0; r < RMAX; r++) {
@@ -243,7 +264,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_count_kernel(Rout
     const int64_t block_base = int64_t(blockIdx.x) * kRouteThreads * a.R;
     const int64_t warp_base = block_base + int64_t(w) * 32 * a.R;
     int er[RMAX];
-    warp_ranks<RMAX>(a.ids, a.n_pairs, E, a.R, warp_base, cnt, er, a.status);
+    warp_ranks<RMAX>(a.ids, a.ids64, a.ids_out, a.n_pairs, E, a.R, warp_base, cnt, er, a.status);
     __syncthreads();
     scan_warps(cnt, hist, E);
     __syncthreads();
@@ -279,7 +300,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteAr
     int d_first = -1, e_first = -1;
     if (i0 + tid < i1) {
         d_first = a.src2dst[i0 + tid];
-        e_first = __ldg(a.ids + i0 + tid);
+        e_first = read_id(a.ids, a.ids64, i0 + tid);
     }
 
     // every block reads the whole table: G threads per column, each a contiguous run of
@@ -315,13 +336,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteAr
         tot[tid] = q;
     }
     __syncthreads();
-    finish_histogram(tot, seg, warp_sums, E, a.P, a.M, a.seg_indptr, a.masked_m, a.partition_counts,
-                     a.status, b == 0);
+    finish_histogram(tot, seg, warp_sums, E, a.P, a.M, a.A, a.seg_indptr, a.masked_m, a.partition_counts,
+                     a.reorder, a.status, b == 0);
 
     for (int64_t i = i0 + tid; i < i1; i += blockDim.x) {
         const bool first = i == i0 + tid;
         const int d = first ? d_first : a.src2dst[i];
-        const int e = first ? e_first : __ldg(a.ids + i);
+        const int e = first ? e_first : read_id(a.ids, a.ids64, i);
         if (d >= 0) {
             const int dst = seg[e] + pre[e] + d;
             a.src2dst[i] = dst;
@@ -380,10 +401,14 @@ RoutePlan plan_route_meta(int64_t n_pairs, int num_experts) {
 cudaError_t launch_route_meta(const LaunchCtx& ctx, const RoutePlan& plan, const int32_t* topk_ids,
                               int64_t n_pairs, int K, int E, int P, int M, int64_t* seg_indptr,
                               int32_t* src2dst, int32_t* reorder_topk_ids, int32_t* masked_m,
-                              int32_t* partition_counts, void* workspace, int32_t* dev_status) {
+                              int32_t* partition_counts, void* workspace, int32_t* dev_status, int A,
+                              const int64_t* topk_ids64, int32_t* ids_out) {
     (void)K;
     RouteArgs a{};
-    a.ids = topk_ids;
+    a.A = A;
+    a.ids = topk_ids64 ? nullptr : topk_ids;
+    a.ids64 = topk_ids64;
+    a.ids_out = ids_out;
     a.n_pairs = n_pairs;
     a.E = E;
     a.P = P;

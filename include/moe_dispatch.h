@@ -66,8 +66,21 @@ typedef enum { MOE_MODE_NORMAL = 0, MOE_MODE_MASKED = 1 } moe_mode_t;
 typedef enum {
     MOE_QUANT_NONE = 0,        /* bf16 rows                                                  */
     MOE_QUANT_FP8_G128 = 1,    /* e4m3 rows [.., H] + fp32 scales [.., H/128]                */
-    MOE_QUANT_NVFP4_B16 = 2    /* e2m1 rows [.., H/2] (2 per byte) + e4m3 scales [.., H/16]  */
+    MOE_QUANT_NVFP4_B16 = 2,   /* e2m1 rows [.., H/2] (2 per byte) + e4m3 scales [.., H/16]  */
+    MOE_QUANT_FP8_G128_UE8M0 = 3, /* e4m3 rows [.., H] + power-of-two scales as UE8M0 bytes
+                                    [.., H/128] (four groups = one little-endian int32)      */
+    MOE_QUANT_FP8_PASSTHROUGH = 4 /* hidden_states already hold one-byte codes ([T, H] bytes,
+                                    per-tensor FP8): rows of H bytes are copied, no scales   */
 } moe_quant_t;
+
+/* Layout of the FP8 scale arrays (moe_dispatch_ex). */
+typedef enum {
+    MOE_SCALES_ROW_MAJOR = 0,  /* [rows, G]: group g of row r at r*G + g                      */
+    MOE_SCALES_COL_MAJOR = 1   /* MN-major, TMA-aligned: group g of row r at g*R4 + r with R4 =
+                                  rows rounded up to a multiple of 4 (per expert [E, G, R4] in
+                                  the masked layout, R4 from M); UE8M0 bytes: int32 word
+                                  (r, g/4) at (g/4)*R4 + r, byte g%4 of the word              */
+} moe_scale_layout_t;
 
 #define MOE_MAX_EXPERTS 1024   /* E <= 1024                                  */
 #define MOE_MAX_TOPK 16        /* 1 <= K <= 16                               */
@@ -131,6 +144,34 @@ moe_status_t moe_route_meta(const int32_t *topk_ids, int64_t num_tokens, int top
                             int32_t *dev_status, moe_stream_t stream);
 
 /*
+ * moe_route_meta_ex -- moe_route_meta with expert-aligned segments.
+ *
+ * buffer.dispatch(..., expert_alignment=128 if DeepGEMM else 1) in
+ * _DeepEPDispatcherImplNormal._dispatch_core ("sglang token_dispatcher/deepep.py" page):
+ * every expert's segment of the contiguous layout starts at a multiple of
+ * expert_alignment A (1..1024):
+ *   seg_indptr[e+1]     = seg_indptr[e] + roundup(count[e], A)
+ *   src2dst[i]          = seg_indptr[id_i] + #{j < i valid : id_j = id_i}
+ *   reorder_topk_ids[r] = the expert of row r, -1 on the padding rows of each segment
+ *                         (seg_indptr[E] entries; capacity T*K + E*(A-1))
+ *   masked_m[e] and partition_counts[p] count valid pairs (no padding).
+ * A = 1 is moe_route_meta. Padding rows of a dispatched buffer are never written.
+ *
+ * topk_ids may be int32 (topk_ids_bytes = 4) or int64 (8; the pages convert topk_ids with
+ * .to(torch.int64) before dispatch). An int64 id outside [-1, E) is skipped and reported
+ * like any bad id. topk_ids_i32_out ([T*K] int32, or NULL) receives the ids as int32 for the
+ * calls that read int32 ids (ids outside the int32 range become INT32_MIN / INT32_MAX,
+ * which those calls skip and report).
+ * Other arguments, workspace and errors as moe_route_meta; T*K + E*(A-1) <= INT32_MAX.
+ */
+moe_status_t moe_route_meta_ex(const void *topk_ids, int topk_ids_bytes, int64_t num_tokens, int topk,
+                               int num_experts, int num_partitions, int max_tokens_per_expert,
+                               int expert_alignment, int64_t *seg_indptr, int32_t *src2dst,
+                               int32_t *reorder_topk_ids, int32_t *masked_m, int32_t *partition_counts,
+                               int32_t *topk_ids_i32_out, int32_t *expected_m_host, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_status, moe_stream_t stream);
+
+/*
  * moe_route_meta_noalloc -- moe_route_meta without a caller-provided workspace.
  *
  * The pages have no counterpart: this is an addition for callers that cannot allocate
@@ -177,11 +218,17 @@ moe_status_t moe_route_meta_noalloc(const int32_t *topk_ids, int64_t num_tokens,
  *   (MOE_QUANT_NVFP4_B16):  sf = e4m3_rn_satfinite((amax / 6) * g),
  *       q = e2m1_rn_satfinite(x * (g / sf)), all codes 0 when sf decodes to 0;
  *       two codes per byte, the even element in the low nibble; sf row-major [H/16].
+ *   MOE_QUANT_FP8_G128_UE8M0 is FP8_G128 with s rounded up to a power of two 2^k
+ *   (round_scale / use_ue8m0 on the deepep.py page): q = e4m3_rn_satfinite(x / 2^k),
+ *   scale byte = k + 127, [rows, H/128] bytes (= [rows, H/512] little-endian int32).
+ *   MOE_QUANT_FP8_PASSTHROUGH: hidden_states are [T, H] one-byte codes (per-tensor FP8,
+ *   the diff page's gateup_input of fp8_dtype) and each destination row is a copy of H bytes.
  *   All arithmetic is binary32 with round-to-nearest-even, in the order written.
  *
  * Arguments:
- *   hidden_states  [T, H] bf16, 16-byte aligned.
- *   hidden (H)     > 0, H % 16 == 0; H % 128 == 0 for MOE_QUANT_FP8_G128.
+ *   hidden_states  [T, H] bf16 ([T, H] bytes for MOE_QUANT_FP8_PASSTHROUGH), 16-byte aligned.
+ *   hidden (H)     > 0, H % 16 == 0; H % 128 == 0 for the FP8 modes; H % 32 == 0 for
+ *                  MOE_QUANT_FP8_PASSTHROUGH.
  *   topk_ids       [T, K] int32 (read in masked mode; may be NULL in normal mode).
  *   max_tokens_per_expert (M)  >= 1 in masked mode; ignored in normal mode.
  *   src2dst        [T*K] int32 and seg_indptr [E+1] int64 from moe_route_meta
@@ -197,6 +244,29 @@ moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t *hi
                           int num_experts, int max_tokens_per_expert, const int32_t *src2dst,
                           const int64_t *seg_indptr, float input_global_scale, void *out_q,
                           void *out_scales, int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_dispatch_ex -- moe_dispatch with a scale layout and an explicit row capacity.
+ *
+ * For the DeepGEMM consumers of the deepep.py page (sglang_per_token_group_quant_fp8 with
+ * column_major_scales / scale_tma_aligned / scale_ue8m0 in
+ * _DeepEPDispatcherImplNormal.dispatch_a; round_scale / use_ue8m0 in
+ * _DeepEPDispatcherImplLowLatency._dispatch_core):
+ *   scale_layout  MOE_SCALES_ROW_MAJOR (as moe_dispatch) or MOE_SCALES_COL_MAJOR (FP8 modes
+ *                 only): group g of row r at g*R4 + r, R4 = roundup(out_rows, 4) in the
+ *                 normal layout; per expert [E, G, R4] with R4 = roundup(M, 4) in the masked
+ *                 layout. UE8M0 bytes are grouped four per int32 word, the words laid out
+ *                 the same way ([G/4 rounded up, R4] words per expert / buffer).
+ *   out_rows      normal layout: the row capacity of out_q (>= T*K; T*K + E*(A-1) for
+ *                 metadata from moe_route_meta_ex); 0 means T*K. Ignored in masked mode.
+ * Everything else as moe_dispatch.
+ */
+moe_status_t moe_dispatch_ex(moe_mode_t mode, moe_quant_t quant, moe_scale_layout_t scale_layout,
+                             const uint16_t *hidden_states, int64_t num_tokens, int hidden,
+                             const int32_t *topk_ids, int topk, int num_experts, int max_tokens_per_expert,
+                             int64_t out_rows, const int32_t *src2dst, const int64_t *seg_indptr,
+                             float input_global_scale, void *out_q, void *out_scales, int32_t *dev_status,
+                             moe_stream_t stream);
 
 /*
  * moe_route_dispatch -- moe_route_meta followed by moe_dispatch, in one call.
@@ -323,6 +393,16 @@ moe_status_t moe_combine_partitioned(const uint16_t *partial, int64_t num_tokens
  */
 moe_status_t moe_convert_probe(const float *in, int64_t n, uint8_t *e4m3, uint8_t *e2m1,
                                float *e4m3_value, moe_stream_t stream);
+
+/*
+ * moe_combine_ex -- moe_combine with the row capacity of expert_out in the normal layout
+ * (>= T*K; T*K + E*(A-1) for metadata from moe_route_meta_ex; 0 means T*K), so that rows of
+ * expert-aligned segments are accepted. Everything else as moe_combine.
+ */
+moe_status_t moe_combine_ex(moe_mode_t mode, const uint16_t *expert_out, int64_t num_tokens, int hidden,
+                            int topk, int num_experts, int max_tokens_per_expert, int64_t expert_out_rows,
+                            const int32_t *topk_ids, const int32_t *src2dst, const int64_t *seg_indptr,
+                            const float *topk_weights, uint16_t *out, int32_t *dev_status, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -105,7 +105,8 @@ def test_dispatch_and_combine_argument_validation(lib):
         return d(mode, quant, x, T, H, ids, K, E, M, s2d, seg, 1.0, q, s, st, None)
 
     assert disp(mode=2) == 1
-    assert disp(quant=3) == 1
+    assert disp(quant=7) == 1
+    assert disp(quant=3, H=272) == 1                 # UE8M0 FP8 needs H % 128
     assert disp(H=100) == 1                          # H % 16
     assert disp(quant=1, H=272) == 1                 # fp8 needs H % 128
     assert disp(mode=1, M=0) == 1                    # masked needs M >= 1

@@ -1,0 +1,230 @@
+"""GPU parity of the DeepGEMM consumer formats against the oracle: expert-aligned metadata
+(moe_route_meta_ex), FP8 group-128 with power-of-two UE8M0 scales, and the column-major
+(MN-major, TMA-aligned) scale layouts of moe_dispatch_ex; combine over aligned segments
+(moe_combine_ex). All integer and quantised outputs bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import make_case, random_bf16
+
+from _harness import SENTINEL, bytes_of, check_combine, filled, moe, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,E,K,A", [(100, 16, 4, 128), (3000, 37, 8, 8), (64, 8, 2, 1), (20000, 256, 8, 128)])
+def test_aligned_route_meta_matches_oracle(T, E, K, A):
+    m = moe()
+    w = make_case(T, 16, E, K, seed=T + A, routing="zipf" if E >= K else "replace", invalid_rate=0.05)
+    _, ids, _ = to_dev(w)
+    cap = T * K + E * (A - 1)
+    seg = torch.empty(E + 1, dtype=torch.int64, device="cuda")
+    s2d = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    reo = torch.full((cap,), -7, dtype=torch.int32, device="cuda")
+    mm = torch.empty(E, dtype=torch.int32, device="cuda")
+    pc = torch.empty(1, dtype=torch.int32, device="cuda")
+    st = m.new_status()
+    m.moe_route_meta_ex(ids, E, seg, s2d, reo, mm, st, m.new_workspace(T, K, E), 1, 0, A, pc)
+    om = oracle.route_meta_aligned(w.topk_ids, E, A)
+    torch.cuda.synchronize()
+    n = int(om.seg_indptr[-1])
+    assert np.array_equal(seg.cpu().numpy(), om.seg_indptr)
+    assert np.array_equal(s2d.cpu().numpy(), om.src2dst)
+    assert np.array_equal(reo[:n].cpu().numpy(), om.reorder_topk_ids)
+    assert (reo[n:].cpu().numpy() == -7).all()
+    assert np.array_equal(mm.cpu().numpy(), om.masked_m) and int(pc.item()) == int(om.partition_counts[0])
+    assert int(st.item()) == 0
+
+
+def _colmajor_fp32(rowmajor, R4):
+    rows, G = rowmajor.shape
+    out = np.full((G, R4), SENTINEL * 0x01010101, np.uint32)
+    out[:, :rows] = rowmajor.view(np.uint32).T
+    return out
+
+
+def _colmajor_ue8m0(rowmajor, R4):
+    rows, G = rowmajor.shape
+    G4 = (G + 3) // 4
+    out = np.full((G4, R4, 4), SENTINEL, np.uint8)
+    for g in range(G):
+        out[g // 4, :rows, g % 4] = rowmajor[:, g]
+    return out
+
+
+@pytest.mark.parametrize("quant", ["fp8g128", "fp8g128_ue8m0"])
+@pytest.mark.parametrize("layout", ["row", "col"])
+def test_aligned_dispatch_and_combine(quant, layout):
+    """Normal layout over 128-aligned segments, both scale layouts."""
+    m = moe()
+    T, H, E, K, A = 300, 640, 24, 6, 128
+    w = make_case(T, H, E, K, seed=51, routing="zipf", invalid_rate=0.05)
+    x, ids, wt = to_dev(w)
+    cap = T * K + E * (A - 1)
+    om = oracle.route_meta_aligned(w.topk_ids, E, A)
+    seg = torch.from_numpy(om.seg_indptr).cuda()
+    s2d = torch.from_numpy(om.src2dst).cuda()
+    G = H // 128
+    q = filled((cap, H), torch.uint8)
+    R4 = (cap + 3) // 4 * 4
+    if quant == "fp8g128":
+        scales = filled((cap, G) if layout == "row" else (G, R4), torch.float32)
+    else:
+        scales = filled((cap, G) if layout == "row" else ((G + 3) // 4, R4, 4), torch.uint8)
+    st = m.new_status()
+    m.moe_dispatch_ex("normal", quant, layout, x, ids, E, s2d, seg, q, scales, st, out_rows=cap)
+    torch.cuda.synchronize()
+    gq = q.cpu().numpy()
+    rows_written = np.zeros(cap, bool)
+    ref_scale = np.zeros((cap, G), np.float32 if quant == "fp8g128" else np.uint8)
+    for i, d in enumerate(om.src2dst):
+        if d < 0:
+            continue
+        t = i // K
+        if quant == "fp8g128":
+            oq, os_ = oracle.quant_fp8_row(w.x[t])
+        else:
+            oq, os_ = oracle.quant_fp8_ue8m0_row(w.x[t])
+        assert np.array_equal(gq[d], oq)
+        ref_scale[d] = os_
+        rows_written[d] = True
+    assert (gq[~rows_written] == SENTINEL).all()          # padding rows and unused capacity untouched
+    gs = scales.cpu().numpy()
+    if layout == "row":
+        got = gs[rows_written]
+        want = ref_scale[rows_written]
+        assert np.array_equal(got.view(np.uint8), want.view(np.uint8))
+    else:
+        if quant == "fp8g128":
+            full = _colmajor_fp32(np.where(rows_written[:, None], ref_scale, np.float32(0)).astype(np.float32), R4)
+            mask = np.zeros((G, R4), bool)
+            mask[:, :cap] = rows_written[None, :]
+            assert np.array_equal(gs.view(np.uint32)[mask], full[mask])
+            assert (gs.view(np.uint32)[~mask] == SENTINEL * 0x01010101).all()
+        else:
+            full = _colmajor_ue8m0(ref_scale, R4)
+            mask = np.zeros(((G + 3) // 4, R4, 4), bool)
+            for g in range(G):
+                mask[g // 4, :cap, g % 4] = rows_written
+            assert np.array_equal(gs[mask], full[mask])
+            assert (gs[~mask] == SENTINEL).all()
+    # combine over the aligned rows
+    eo_h = random_bf16(np.random.default_rng(52), (cap, H))
+    eo = torch.from_numpy(eo_h.view(np.int16)).cuda().view(torch.bfloat16)
+    out = filled((T, H), torch.bfloat16)
+    m.moe_combine_ex("normal", eo, ids, wt, E, s2d, seg, out, st, expert_out_rows=cap)
+    meta = oracle.Meta(om.seg_indptr, om.src2dst, om.reorder_topk_ids, om.masked_m, om.partition_counts, 0, 0)
+    want = oracle.combine("normal", eo_h, w.topk_ids, w.topk_weights, meta, E)
+    torch.cuda.synchronize()
+    check_combine(bytes_of(out).view(np.uint16).reshape(T, H), want)
+    assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("quant", ["fp8g128", "fp8g128_ue8m0"])
+def test_masked_colmajor_scales(quant):
+    """Masked layout [E, M, .] with per-expert column-major scales [E, G, roundup(M, 4)]."""
+    m = moe()
+    T, H, E, K, M = 96, 1024, 16, 4, 30
+    w = make_case(T, H, E, K, seed=53, invalid_rate=0.05)
+    x, ids, _ = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, E, M=M)
+    seg = torch.from_numpy(om.seg_indptr).cuda()
+    s2d = torch.from_numpy(om.src2dst).cuda()
+    G, M4 = H // 128, (M + 3) // 4 * 4
+    q = filled((E, M, H), torch.uint8)
+    if quant == "fp8g128":
+        scales = filled((E, G, M4), torch.float32)
+    else:
+        scales = filled((E, (G + 3) // 4, M4, 4), torch.uint8)
+    st = m.new_status()
+    m.moe_dispatch_ex("masked", quant, "col", x, ids, E, s2d, seg, q, scales, st, max_tokens_per_expert=M)
+    torch.cuda.synchronize()
+    gq, gs = q.cpu().numpy(), scales.cpu().numpy()
+    flat = w.topk_ids.reshape(-1)
+    for i, d in enumerate(om.src2dst):
+        if d < 0:
+            continue
+        e, r = int(flat[i]), int(d - om.seg_indptr[flat[i]])
+        if r >= M:
+            continue
+        if quant == "fp8g128":
+            oq, os_ = oracle.quant_fp8_row(w.x[i // K])
+            assert np.array_equal(gs[e, :, r].view(np.uint32), os_.view(np.uint32))
+        else:
+            oq, os_ = oracle.quant_fp8_ue8m0_row(w.x[i // K])
+            assert np.array_equal(np.array([gs[e, g // 4, r, g % 4] for g in range(G)], np.uint8), os_)
+        assert np.array_equal(gq[e, r], oq)
+
+
+def test_ue8m0_through_fused_route_dispatch():
+    """moe_route_dispatch with UE8M0 scales (the fused small-batch kernel), masked layout."""
+    m = moe()
+    w = make_case(128, 7168, 256, 8, seed=54, mode="masked", M=128, routing="softmax")
+    x, ids, _ = to_dev(w)
+    d = m.MoEDispatcher(128, 7168, 8, 256, mode="masked", quant="fp8g128_ue8m0", max_tokens_per_expert=128)
+    d.route_dispatch(x, ids)
+    om = oracle.route_meta(w.topk_ids, 256, M=128)
+    torch.cuda.synchronize()
+    gq, gs = d.out_q.cpu().numpy(), d.out_scales.cpu().numpy()
+    flat = w.topk_ids.reshape(-1)
+    for i, dd in enumerate(om.src2dst):
+        e, r = int(flat[i]), int(dd - om.seg_indptr[flat[i]])
+        oq, os_ = oracle.quant_fp8_ue8m0_row(w.x[i // 8])
+        assert np.array_equal(gq[e, r], oq) and np.array_equal(gs[e, r], os_)
+    d.check()
+
+
+# --- f4: int64 topk_ids and per-tensor FP8 pass-through rows ---------------------------------
+
+@pytest.mark.parametrize("T,K,E", [(128, 8, 256), (5000, 8, 64)])
+def test_int64_ids_match_int32_metadata(T, K, E):
+    m = moe()
+    w = make_case(T, 16, E, K, seed=T + 71, invalid_rate=0.05, bad_rate=0.01)
+    ids64 = w.topk_ids.astype(np.int64)
+    # a few ids whose low 32 bits alias valid experts: they must count as bad, not as experts
+    ids64.reshape(-1)[::97] = (np.int64(1) << 40) + 3
+    want_ids = np.where((ids64 >= -(1 << 31)) & (ids64 < (1 << 31)), ids64, np.int64(1 << 31) - 1).astype(np.int32)
+    om = oracle.route_meta(want_ids, E)
+    d64 = torch.from_numpy(ids64).cuda()
+    seg = torch.empty(E + 1, dtype=torch.int64, device="cuda")
+    s2d = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    reo = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    mm = torch.empty(E, dtype=torch.int32, device="cuda")
+    i32 = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    st = m.new_status()
+    m.moe_route_meta_ex(d64, E, seg, s2d, reo, mm, st, m.new_workspace(T, K, E), topk_ids_i32_out=i32)
+    torch.cuda.synchronize()
+    n = om.num_valid
+    assert np.array_equal(seg.cpu().numpy(), om.seg_indptr)
+    assert np.array_equal(s2d.cpu().numpy(), om.src2dst)
+    assert np.array_equal(reo[:n].cpu().numpy(), om.reorder_topk_ids)
+    assert np.array_equal(i32.cpu().numpy(), want_ids)
+    assert int(st.item()) == m.MOE_ERR_BAD_EXPERT_ID
+
+
+@pytest.mark.parametrize("mode,M", [("normal", 0), ("masked", 64)])
+def test_fp8_passthrough_dispatch(mode, M):
+    m = moe()
+    T, H, E, K = 200, 2048, 32, 4
+    w = make_case(T, H, E, K, seed=72, invalid_rate=0.05)
+    codes = np.random.default_rng(73).integers(0, 256, size=(T, H), dtype=np.uint8)
+    xc = torch.from_numpy(codes).cuda()
+    _, ids, _ = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, E, M=M)
+    seg = torch.from_numpy(om.seg_indptr).cuda()
+    s2d = torch.from_numpy(om.src2dst).cuda()
+    q = filled((T * K, H) if mode == "normal" else (E, M, H), torch.uint8)
+    st = m.new_status()
+    m.moe_dispatch(mode, "fp8_passthrough", xc, ids, E, s2d, seg, q, None, st, M)
+    want, _ = oracle.dispatch(mode, "fp8_passthrough", codes, w.topk_ids, om, E, M=M, fill=SENTINEL)
+    torch.cuda.synchronize()
+    assert np.array_equal(q.cpu().numpy(), want)
+    # the same through the fused small-batch call
+    d = m.MoEDispatcher(T, H, K, E, mode=mode, quant="fp8_passthrough", max_tokens_per_expert=M)
+    d.out_q = filled(tuple(q.shape), torch.uint8)
+    d.route_dispatch(xc, ids)
+    torch.cuda.synchronize()
+    assert np.array_equal(d.out_q.cpu().numpy(), want)
+    d.check()
