@@ -27,6 +27,7 @@
 //    contiguous 1 KB / 512 B / 256 B span of each destination row.
 //  * Grid-stride over units with a grid of (SMs x resident blocks); the warp-to-unit
 //    order walks a token's slices with neighbouring warps.
+#include <algorithm>
 #include <cstdint>
 
 #include "dispatch_slice.cuh"
@@ -39,6 +40,7 @@ namespace {
 constexpr int kDispatchThreads = 256;
 constexpr int kSlice = 512;       // elements per warp unit
 constexpr int kLaneElems = 16;    // elements per lane
+constexpr int64_t kBulkMinTokens = 1024;  // the bulk (TMA) path for batches this large
 
 struct DispatchArgs {
     const uint16_t* x;
@@ -117,8 +119,246 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     }
 }
 
+// ---------------------------------------------------------------------------
+// Bulk (TMA) path for large batches: one token row at a time per CTA. The row is
+// bulk-loaded into a shared-memory ring (mbarrier completion, loads issued NS-1 tokens
+// ahead); the quantising modes turn it into the quantised row + scale row in shared
+// memory; then one bulk store per destination row (and per scale row) writes whole rows.
+// Whole-row bulk stores keep each destination's bytes together in DRAM (a probe of this
+// pattern ran at 5.8 TB/s against 5.0 TB/s for 512-byte warp slices).
+// ---------------------------------------------------------------------------
+struct BulkGeom {
+    uint32_t in_bytes;   // 2H: one bf16 row
+    uint32_t q_bytes;    // quantised row (2H for the copy)
+    uint32_t s_bytes;    // scale row (0 for the copy)
+    uint32_t in_off;     // shared offsets
+    uint32_t out_off;
+    int stages;
+};
+
+constexpr int kBulkCopyThreads = 32;
+constexpr int kBulkQuantThreads = 256;
+constexpr uint32_t kBulkHeader = 512;  // mbarriers (8 B each) and destination rows (2 x 16 x 8 B)
+
+template <bool MASKED>
+__device__ __forceinline__ void stage_seg(const DispatchArgs& a, int* s_seg) {
+    if (MASKED)
+        for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_seg[e] = int(a.seg[e]);
+}
+
+// copy mode: lane 0 drives the ring, lanes < K resolve the destination rows
+template <bool MASKED>
+__global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(DispatchArgs a, BulkGeom geo) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31, NS = geo.stages;
+    const uint32_t bar0 = smem_addr(smem), in0 = smem_addr(smem + geo.in_off);
+    int* s_seg = reinterpret_cast<int*>(smem + geo.out_off);
+    if (lane == 0) {
+        for (int s = 0; s < NS; s++) mbar_init(bar0 + 8 * s, 1);
+        mbar_fence_init();
+    }
+    stage_seg<MASKED>(a, s_seg);
+    __syncwarp();
+    const int64_t G = gridDim.x;
+    const int64_t ntok = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / G + 1 : 0;
+    int64_t issued = 0, consumed = 0;  // lane 0's counts of loads issued / completed
+    auto issue = [&](int64_t i) {
+        const int s = int(i % NS);
+        bulk_load(in0 + s * geo.in_bytes, a.x + (blockIdx.x + i * G) * a.H, geo.in_bytes, bar0 + 8 * s);
+        issued = i + 1;
+    };
+    if (lane == 0)
+        for (int64_t i = 0; i < NS - 1 && i < ntok; i++) issue(i);
+    for (int64_t i = 0; i < ntok; i++) {
+        const int64_t t = blockIdx.x + i * G;
+        const int s = int(i % NS);
+        const int64_t my_row = dest_row<MASKED>(a, s_seg, t, lane);
+        int ok = 1;
+        if (lane == 0) {
+            if (i + NS - 1 < ntok) {
+                bulk_wait_read<0>();  // the stage being refilled was the source of token i-1's stores
+                issue(i + NS - 1);
+            }
+            ok = mbar_wait(bar0 + 8 * s, uint32_t((i / NS) & 1));
+            consumed += ok;
+        }
+        ok = __shfl_sync(kFullMask, ok, 0);
+        if (!ok) {
+            if (lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
+            break;
+        }
+        for (int k = 0; k < a.K; k++) {
+            const int64_t row = __shfl_sync(kFullMask, my_row, k);
+            if (lane == 0 && row >= 0)
+                bulk_store(static_cast<uint8_t*>(a.out_q) + row * geo.q_bytes, in0 + s * geo.in_bytes, geo.q_bytes);
+        }
+        if (lane == 0) bulk_commit();
+    }
+    if (lane == 0) {
+        bulk_wait_all();
+        // after a timeout, loads still in flight are waited for (bounded) before shared memory is released
+        for (int64_t j = consumed; j < issued; j++) mbar_wait(bar0 + 8 * int(j % NS), uint32_t((j / NS) & 1), 1 << 20);
+    }
+}
+
+// quantising modes: 256 threads quantise shared -> shared; thread 0 drives the copies
+template <int QUANT, bool MASKED>
+__global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(DispatchArgs a, BulkGeom geo) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
+    const int NS = geo.stages, H = a.H;
+    const uint32_t bar0 = smem_addr(smem);
+    int64_t* s_rows = reinterpret_cast<int64_t*>(smem + 256);  // [2][16]
+    unsigned char* in_base = smem + geo.in_off;
+    unsigned char* out_base = smem + geo.out_off;                // [2][q_bytes + s_bytes]
+    int* s_seg = reinterpret_cast<int*>(out_base + 2 * (geo.q_bytes + geo.s_bytes));
+    const uint32_t in0 = smem_addr(in_base), out0 = smem_addr(out_base);
+    const uint32_t out_bytes = geo.q_bytes + geo.s_bytes;
+    if (tid == 0) {
+        for (int s = 0; s < NS; s++) mbar_init(bar0 + 8 * s, 1);
+        mbar_fence_init();
+    }
+    stage_seg<MASKED>(a, s_seg);
+    __syncthreads();
+    const int64_t G = gridDim.x;
+    const int64_t ntok = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / G + 1 : 0;
+    int64_t issued = 0, consumed = 0;  // thread 0's counts of loads issued / completed
+    auto issue = [&](int64_t i) {
+        const int s = int(i % NS);
+        bulk_load(in0 + s * geo.in_bytes, a.x + (blockIdx.x + i * G) * H, geo.in_bytes, bar0 + 8 * s);
+        issued = i + 1;
+    };
+    if (tid == 0)
+        for (int64_t i = 0; i < NS - 1 && i < ntok; i++) issue(i);
+    const int nslices = H / kLaneElems;
+    for (int64_t i = 0; i < ntok; i++) {
+        const int64_t t = blockIdx.x + i * G;
+        const int s = int(i % NS), o = int(i & 1);
+        if (warp == 0) {
+            const int64_t r = dest_row<MASKED>(a, s_seg, t, lane);
+            if (lane < a.K) s_rows[o * 16 + lane] = r;
+        }
+        if (tid == 0) {
+            if (i + NS - 1 < ntok) issue(i + NS - 1);  // its stage was last read before the previous barrier
+            bulk_wait_read<1>();                       // out stage o was the source of token i-2's stores
+        }
+        const int ok = __syncthreads_and(mbar_wait(bar0 + 8 * s, uint32_t((i / NS) & 1)));
+        if (!ok) {
+            if (tid == 0) set_status(a.status, MOE_ERR_TIMEOUT);
+            break;
+        }
+        consumed = i + 1;
+        const unsigned char* src = in_base + size_t(s) * geo.in_bytes;
+        unsigned char* qo = out_base + size_t(o) * out_bytes;
+        unsigned char* so = qo + geo.q_bytes;
+        for (int base = warp * 32; base < nslices; base += nthreads) {
+            const int slice = base + lane;
+            const bool active = slice < nslices;
+            LaneSlice sl{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            if (active) {
+                sl.v0 = *reinterpret_cast<const uint4*>(src + slice * 32);
+                sl.v1 = *reinterpret_cast<const uint4*>(src + slice * 32 + 16);
+            }
+            const LaneCodes c = quantise16<QUANT>(sl, a.g);
+            if (active) {
+                if constexpr (QUANT == MOE_QUANT_NVFP4_B16) {
+                    *reinterpret_cast<uint2*>(qo + slice * 8) = make_uint2(c.q.x, c.q.y);
+                    so[slice] = uint8_t(c.scale);
+                } else {
+                    *reinterpret_cast<uint4*>(qo + slice * 16) = c.q;
+                    if ((lane & 7) == 0) {
+                        if constexpr (QUANT == MOE_QUANT_FP8_G128)
+                            reinterpret_cast<uint32_t*>(so)[slice / 8] = c.scale;
+                        else
+                            so[slice / 8] = uint8_t(c.scale);
+                    }
+                }
+            }
+        }
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+            for (int k = 0; k < a.K; k++) {
+                const int64_t row = s_rows[o * 16 + k];
+                if (row < 0) continue;
+                bulk_store(static_cast<uint8_t*>(a.out_q) + row * geo.q_bytes, out0 + o * out_bytes, geo.q_bytes);
+                bulk_store(static_cast<uint8_t*>(a.out_s) + row * geo.s_bytes, out0 + o * out_bytes + geo.q_bytes,
+                           geo.s_bytes);
+            }
+            bulk_commit();
+        }
+    }
+    if (tid == 0) {
+        bulk_wait_all();
+        // after a timeout, loads still in flight are waited for (bounded) before shared memory is released
+        for (int64_t j = consumed; j < issued; j++) mbar_wait(bar0 + 8 * int(j % NS), uint32_t((j / NS) & 1), 1 << 20);
+    }
+}
+
+// Row geometry of the bulk path, or stages = 0 when it does not apply (rows or scale rows
+// that are not 16-byte multiples, unaligned bases, column-major scales, shared memory).
+BulkGeom bulk_geometry(int quant, const DispatchArgs& a) {
+    BulkGeom g{};
+    const int H = a.H;
+    g.in_bytes = uint32_t(2 * H);
+    switch (quant) {
+        case MOE_QUANT_NONE: g.q_bytes = uint32_t(2 * H); g.s_bytes = 0; break;
+        case MOE_QUANT_FP8_G128: g.q_bytes = uint32_t(H); g.s_bytes = uint32_t(H / 32); break;
+        case MOE_QUANT_FP8_G128_UE8M0: g.q_bytes = uint32_t(H); g.s_bytes = uint32_t(H / 128); break;
+        default: g.q_bytes = uint32_t(H / 2); g.s_bytes = uint32_t(H / 16); break;
+    }
+    const bool aligned16 = (reinterpret_cast<uintptr_t>(a.out_s) & 15) == 0;
+    if (g.q_bytes % 16 || g.s_bytes % 16 || a.L.col_major || (quant != MOE_QUANT_NONE && !aligned16)) return g;
+    const uint32_t seg_bytes = uint32_t(sizeof(int)) * uint32_t(a.E);
+    const int stages = quant == MOE_QUANT_NONE ? 4 : 3;
+    g.in_off = kBulkHeader;
+    g.out_off = g.in_off + uint32_t(stages) * g.in_bytes;
+    const size_t smem = size_t(g.out_off) + (quant == MOE_QUANT_NONE ? 0 : 2 * (g.q_bytes + g.s_bytes)) + seg_bytes;
+    if (smem > 200 * 1024) return g;
+    g.stages = stages;
+    return g;
+}
+
+size_t bulk_smem(int quant, const BulkGeom& g, int E) {
+    return size_t(g.out_off) + (quant == MOE_QUANT_NONE ? 0 : 2 * (g.q_bytes + g.s_bytes)) + sizeof(int) * size_t(E);
+}
+
+template <int QUANT, bool MASKED>
+cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkGeom& geo) {
+    const size_t smem = bulk_smem(QUANT, geo, a.E);
+    int threads;
+    int per_sm = 0;
+    cudaError_t err;
+    if constexpr (QUANT == MOE_QUANT_NONE) {
+        auto kern = dispatch_bulk_copy_kernel<MASKED>;
+        threads = kBulkCopyThreads;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err == cudaSuccess) err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
+        if (err != cudaSuccess) return err;
+        const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * per_sm));
+        return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
+    } else {
+        auto kern = dispatch_bulk_quant_kernel<QUANT, MASKED>;
+        threads = kBulkQuantThreads;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err == cudaSuccess) err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
+        if (err != cudaSuccess) return err;
+        const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * per_sm));
+        return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
+    }
+}
+
 template <int QUANT, bool MASKED>
 cudaError_t launch_variant(const LaunchCtx& ctx, const DispatchArgs& a) {
+    // large batches: the bulk path when its geometry applies
+    if (a.T >= kBulkMinTokens) {
+        const BulkGeom geo = bulk_geometry(QUANT, a);
+        if (geo.stages > 0) return launch_bulk<QUANT, MASKED>(ctx, a, geo);
+    }
     auto kern = dispatch_kernel<QUANT, MASKED>;
     const size_t smem = MASKED ? sizeof(int) * size_t(a.E) : 0;
     // one wave or less of 256-thread blocks leaves SMs unevenly loaded: use 64 threads

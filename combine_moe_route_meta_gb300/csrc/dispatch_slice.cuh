@@ -50,6 +50,73 @@ __device__ __forceinline__ LaneSlice load_slice(const uint16_t* src) {
     return s;
 }
 
+// The quantised form of one lane's 16 elements.
+//   FP8 (both scale kinds): q = 16 e4m3 codes; scale = fp32 scale bits or the UE8M0 byte
+//   NVFP4: q.x, q.y = 16 e2m1 codes (8 bytes); scale = the e4m3 block-scale byte
+struct LaneCodes {
+    uint4 q;
+    uint32_t scale;
+};
+
+// Quantise the lane's 16 elements. FP8 modes reduce amax over the 8 aligned lanes of a
+// 128-element group with shuffles, so all 32 lanes of the warp must call this together
+// (inactive lanes hold zeros, and a group is never split between active and inactive lanes).
+template <int QUANT>
+__device__ __forceinline__ LaneCodes quantise16(const LaneSlice& s, float g) {
+    float f[16];
+    unpack8(s.v0, f);
+    unpack8(s.v1, f + 8);
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
+    LaneCodes out;
+    if constexpr (QUANT == MOE_QUANT_FP8_G128 || QUANT == MOE_QUANT_FP8_G128_UE8M0) {
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+        const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+        uint32_t w[4];
+        if constexpr (QUANT == MOE_QUANT_FP8_G128) {
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                const uint32_t lo = e4m3x2(__fdiv_rn(f[4 * p], sc), __fdiv_rn(f[4 * p + 1], sc));
+                const uint32_t hi = e4m3x2(__fdiv_rn(f[4 * p + 2], sc), __fdiv_rn(f[4 * p + 3], sc));
+                w[p] = lo | (hi << 16);
+            }
+            out.scale = __float_as_uint(sc);
+        } else {
+            // the scale rounded up to a power of two 2^(ex-127): dividing by it is exact, so
+            // x * 2^(127-ex) gives the same binary32 value as x / 2^(ex-127)
+            const uint32_t bits = __float_as_uint(sc);
+            const uint32_t ex = (bits >> 23) + ((bits & 0x7fffffu) ? 1u : 0u);
+            const float inv = __uint_as_float((254u - ex) << 23);
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+                const uint32_t lo = e4m3x2(__fmul_rn(f[4 * p], inv), __fmul_rn(f[4 * p + 1], inv));
+                const uint32_t hi = e4m3x2(__fmul_rn(f[4 * p + 2], inv), __fmul_rn(f[4 * p + 3], inv));
+                w[p] = lo | (hi << 16);
+            }
+            out.scale = ex;
+        }
+        out.q = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {  // MOE_QUANT_NVFP4_B16: the lane's 16 elements are one block
+        const float tsf = __fmul_rn(__fdiv_rn(amax, 6.0f), g);
+        const uint32_t sf = e4m3x2(tsf, 0.0f) & 0xffu;
+        const float sff = e4m3_value(sf);
+        out.q = make_uint4(0, 0, 0, 0);
+        if (sff != 0.0f) {
+            const float r = __fdiv_rn(g, sff);
+            uint32_t b[8];
+#pragma unroll
+            for (int p = 0; p < 8; p++) b[p] = e2m1x2(__fmul_rn(f[2 * p], r), __fmul_rn(f[2 * p + 1], r));
+            out.q.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+            out.q.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+        }
+        out.scale = sf;
+    }
+    return out;
+}
+
 // Quantise `s` (the lane's 16 elements starting at column `col`, lane index `lane`) and
 // write it to every destination row: row k of the token is __shfl(my_row, k), -1 = none.
 // All 32 lanes of the warp must call this together (the FP8 group amax and the row
@@ -68,96 +135,24 @@ __device__ __forceinline__ void quantise_store(const LaneSlice& s, bool active, 
                 st_v4(dst + 8, s.v1);
             }
         }
-    } else if constexpr (QUANT == MOE_QUANT_FP8_G128) {
-        float f[16];
-        unpack8(s.v0, f);
-        unpack8(s.v1, f + 8);
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
-        // a 128-element group is 8 aligned lanes
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-        const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-        uint32_t w[4];
-#pragma unroll
-        for (int p = 0; p < 4; p++) {
-            const uint32_t lo = e4m3x2(__fdiv_rn(f[4 * p], sc), __fdiv_rn(f[4 * p + 1], sc));
-            const uint32_t hi = e4m3x2(__fdiv_rn(f[4 * p + 2], sc), __fdiv_rn(f[4 * p + 3], sc));
-            w[p] = lo | (hi << 16);
-        }
-        const uint4 q = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        const LaneCodes c = quantise16<QUANT>(s, g);
         uint8_t* out = static_cast<uint8_t*>(out_q);
-        float* scales = static_cast<float*>(out_s);
         const int groups = H / 128;
         for (int k = 0; k < K; k++) {
             const int64_t row = __shfl_sync(kFullMask, my_row, k);
-            if (row >= 0 && active) {
-                st_v4(out + row * H + col, q);
-                if ((lane & 7) == 0) scales[scale_index(L, row, col / 128, groups, false)] = sc;
-            }
-        }
-    } else if constexpr (QUANT == MOE_QUANT_FP8_G128_UE8M0) {
-        // as FP8 g128, with the scale rounded up to a power of two 2^(ex-127): dividing by it
-        // is exact, so x * 2^(127-ex) gives the same binary32 value as x / 2^(ex-127)
-        float f[16];
-        unpack8(s.v0, f);
-        unpack8(s.v1, f + 8);
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-        const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-        const uint32_t bits = __float_as_uint(sc);
-        const uint32_t ex = (bits >> 23) + ((bits & 0x7fffffu) ? 1u : 0u);
-        const float inv = __uint_as_float((254u - ex) << 23);
-        uint32_t w[4];
-#pragma unroll
-        for (int p = 0; p < 4; p++) {
-            const uint32_t lo = e4m3x2(__fmul_rn(f[4 * p], inv), __fmul_rn(f[4 * p + 1], inv));
-            const uint32_t hi = e4m3x2(__fmul_rn(f[4 * p + 2], inv), __fmul_rn(f[4 * p + 3], inv));
-            w[p] = lo | (hi << 16);
-        }
-        const uint4 q = make_uint4(w[0], w[1], w[2], w[3]);
-        uint8_t* out = static_cast<uint8_t*>(out_q);
-        uint8_t* sfo = static_cast<uint8_t*>(out_s);
-        const int groups = H / 128;
-        for (int k = 0; k < K; k++) {
-            const int64_t row = __shfl_sync(kFullMask, my_row, k);
-            if (row >= 0 && active) {
-                st_v4(out + row * H + col, q);
-                if ((lane & 7) == 0) sfo[scale_index(L, row, col / 128, groups, true)] = uint8_t(ex);
-            }
-        }
-    } else {  // MOE_QUANT_NVFP4_B16
-        float f[16];
-        unpack8(s.v0, f);
-        unpack8(s.v1, f + 8);
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; j++) amax = fmaxf(amax, fabsf(f[j]));
-        const float tsf = __fmul_rn(__fdiv_rn(amax, 6.0f), g);
-        const uint32_t sf = e4m3x2(tsf, 0.0f) & 0xffu;
-        const float sff = e4m3_value(sf);
-        uint2 q = make_uint2(0, 0);
-        if (sff != 0.0f) {
-            const float r = __fdiv_rn(g, sff);
-            uint32_t b[8];
-#pragma unroll
-            for (int p = 0; p < 8; p++) b[p] = e2m1x2(__fmul_rn(f[2 * p], r), __fmul_rn(f[2 * p + 1], r));
-            q.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-            q.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
-        }
-        uint8_t* out = static_cast<uint8_t*>(out_q);
-        uint8_t* sfo = static_cast<uint8_t*>(out_s);
-        for (int k = 0; k < K; k++) {
-            const int64_t row = __shfl_sync(kFullMask, my_row, k);
-            if (row >= 0 && active) {
-                st_v2(out + row * (H / 2) + col / 2, q);
-                sfo[row * (H / 16) + col / 16] = uint8_t(sf);
+            if (row < 0 || !active) continue;
+            if constexpr (QUANT == MOE_QUANT_FP8_G128) {
+                st_v4(out + row * H + col, c.q);
+                if ((lane & 7) == 0)
+                    static_cast<float*>(out_s)[scale_index(L, row, col / 128, groups, false)] = __uint_as_float(c.scale);
+            } else if constexpr (QUANT == MOE_QUANT_FP8_G128_UE8M0) {
+                st_v4(out + row * H + col, c.q);
+                if ((lane & 7) == 0)
+                    static_cast<uint8_t*>(out_s)[scale_index(L, row, col / 128, groups, true)] = uint8_t(c.scale);
+            } else {
+                st_v2(out + row * (H / 2) + col / 2, make_uint2(c.q.x, c.q.y));
+                static_cast<uint8_t*>(out_s)[row * (H / 16) + col / 16] = uint8_t(c.scale);
             }
         }
     }

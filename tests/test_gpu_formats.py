@@ -228,3 +228,28 @@ def test_fp8_passthrough_dispatch(mode, M):
     torch.cuda.synchronize()
     assert np.array_equal(d.out_q.cpu().numpy(), want)
     d.check()
+
+
+def test_ue8m0_bulk_path_normal_layout():
+    """>= 1024 tokens with 16-byte UE8M0 scale rows (H = 2048): the bulk dispatch path."""
+    m = moe()
+    T, H, E, K = 1200, 2048, 64, 8
+    w = make_case(T, H, E, K, seed=81, routing="zipf", invalid_rate=0.05)
+    x, ids, _ = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, E)
+    seg = torch.from_numpy(om.seg_indptr).cuda()
+    s2d = torch.from_numpy(om.src2dst).cuda()
+    q = filled((T * K, H), torch.uint8)
+    sc = filled((T * K, H // 128), torch.uint8)
+    st = m.new_status()
+    m.moe_dispatch("normal", "fp8g128_ue8m0", x, ids, E, s2d, seg, q, sc, st)
+    torch.cuda.synchronize()
+    gq, gs = q.cpu().numpy(), sc.cpu().numpy()
+    for i, d in enumerate(om.src2dst):
+        if d < 0:
+            continue
+        oq, oe = oracle.quant_fp8_ue8m0_row(w.x[i // K])
+        assert np.array_equal(gq[d], oq) and np.array_equal(gs[d], oe)
+    n = om.num_valid
+    assert (gq[n:] == SENTINEL).all() and (gs[n:] == SENTINEL).all()
+    assert int(st.item()) == 0

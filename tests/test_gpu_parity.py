@@ -76,6 +76,11 @@ def test_qwen3_masked_secondary():
     (3000, 128, 8, 8, "masked", "none", 3000),     # several route blocks with E < 32
     (1200, 128, 1024, 16, "normal", "none", 0),    # E and K at their limits, several blocks
     (40, 128, 1024, 16, "masked", "fp8g128", 8),   # E = 1024 in one block
+    # >= 1024 tokens with 16-byte row geometry: the bulk (TMA) dispatch path
+    (1500, 1024, 64, 8, "normal", "fp8g128", 0),
+    (1100, 2048, 32, 6, "masked", "nvfp4b16", 400),
+    (1030, 512, 16, 4, "masked", "none", 500),
+    (2048, 4096, 128, 8, "normal", "none", 0),
 ])
 def test_shapes_full(T, H, E, K, mode, quant, M):
     w = make_case(T, H, E, K, seed=T + H + E + K, mode=mode, quant=quant, M=M, invalid_rate=0.05)
