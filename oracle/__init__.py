@@ -216,16 +216,21 @@ def _filled(shape, dtype, fill: int) -> np.ndarray:
 
 
 def dispatch(mode: str, quant: str, x: np.ndarray, topk_ids: np.ndarray, meta: Meta, E: int,
-             M: int = 0, global_scale: float = 0.0, rows: Optional[int] = None, fill: int = 0):
+             M: int = 0, global_scale: float = 0.0, rows: Optional[int] = None, fill: int = 0, out=None):
     """Returns (q, scales) in the layout of ``mode``; untouched bytes hold ``fill``.
-    For quant "fp8_passthrough" x is [T, H] uint8 codes."""
+    For quant "fp8_passthrough" x is [T, H] uint8 codes. ``out`` = (q, scales) reuses
+    caller-owned arrays of the right shapes (their untouched bytes are left as they are)."""
     x = np.ascontiguousarray(x, dtype=np.uint8 if quant == "fp8_passthrough" else np.uint16)
     ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
     T, H = x.shape
     K = ids.shape[1]
     qs, qd, ss, sd = out_shapes(mode, quant, T, H, K, E, M, rows)
-    q = _filled(qs, qd, fill)
-    s = _filled(ss, sd, fill) if ss is not None else None
+    if out is not None:
+        q, s = out
+        assert q.shape == qs and q.dtype == qd and (ss is None or (s.shape == ss and s.dtype == sd))
+    else:
+        q = _filled(qs, qd, fill)
+        s = _filled(ss, sd, fill) if ss is not None else None
     _load().oracle_dispatch(MODES[mode], QUANTS[quant], _ptr(x), T, H, _ptr(ids), K, E, M,
                             _ptr(meta.src2dst), _ptr(meta.seg_indptr), float(global_scale),
                             _ptr(q), _ptr(s))
