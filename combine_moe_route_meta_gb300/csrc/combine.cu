@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
     int64_t u = warp;
     SlotMeta meta = load_slot<MASKED>(a, u < a.n_units ? u / a.units_per_row : 0, u < a.n_units ? lane : 32);
     if (MASKED) {
-        for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_seg[e] = int(a.seg[e]);
+        stage_to_shared(a.seg, s_seg, a.E);
         __syncthreads();
     }
 
@@ -165,7 +165,7 @@ cudaError_t launch_variant(const LaunchCtx& ctx, const CombineArgs& a) {
     if (err != cudaSuccess) return err;
     const int64_t warps_per_block = threads / 32;
     const int64_t need = (a.n_units + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = int64_t(ctx.num_sms) * per_sm;
+    const int64_t cap = int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = int(need < cap ? need : cap);
 
     return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a);

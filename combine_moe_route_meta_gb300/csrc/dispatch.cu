@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
     LaneSlice sl{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     if (active) sl = load_slice(a.x + t * H + col);
     if (MASKED) {
-        for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_seg[e] = int(a.seg[e]);
+        stage_to_shared(a.seg, s_seg, a.E);
         __syncthreads();
     }
 
@@ -143,7 +143,7 @@ constexpr uint32_t kBulkHeader = 512;  // mbarriers (8 B each) and destination r
 template <bool MASKED>
 __device__ __forceinline__ void stage_seg(const DispatchArgs& a, int* s_seg) {
     if (MASKED)
-        for (int e = threadIdx.x; e < a.E; e += blockDim.x) s_seg[e] = int(a.seg[e]);
+        stage_to_shared(a.seg, s_seg, a.E);
 }
 
 // copy mode: lane 0 drives the ring, lanes < K resolve the destination rows
@@ -339,7 +339,7 @@ cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkG
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err == cudaSuccess) err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
         if (err != cudaSuccess) return err;
-        const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * per_sm));
+        const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1)));
         return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
     } else {
         auto kern = dispatch_bulk_quant_kernel<QUANT, MASKED>;
@@ -347,7 +347,7 @@ cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkG
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err == cudaSuccess) err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
         if (err != cudaSuccess) return err;
-        const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * per_sm));
+        const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1)));
         return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
     }
 }
@@ -368,7 +368,7 @@ cudaError_t launch_variant(const LaunchCtx& ctx, const DispatchArgs& a) {
     if (err != cudaSuccess) return err;
     const int64_t warps_per_block = threads / 32;
     const int64_t need = (a.n_units + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = int64_t(ctx.num_sms) * per_sm;
+    const int64_t cap = int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = int(need < cap ? need : cap);
 
     return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a);

@@ -96,6 +96,28 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
 }
 
 // ---------------------------------------------------------------------------
+// block-wide staging of small metadata arrays into shared memory
+// ---------------------------------------------------------------------------
+// Each thread issues all of its loads (up to 8) before any of its stores, so the copy costs
+// one memory round trip; a plain strided loop would wait for every load in turn.
+template <typename Src>
+__device__ __forceinline__ void stage_to_shared(const Src* __restrict__ src, int* dst, int n) {
+    for (int j0 = threadIdx.x; j0 < n; j0 += 8 * int(blockDim.x)) {
+        Src v[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int j = j0 + u * int(blockDim.x);
+            v[u] = j < n ? __ldg(src + j) : Src(0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int j = j0 + u * int(blockDim.x);
+            if (j < n) dst[j] = int(v[u]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // bulk (TMA) copies and mbarriers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

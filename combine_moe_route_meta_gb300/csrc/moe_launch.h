@@ -37,23 +37,32 @@ cudaError_t launch_pdl(const LaunchCtx& ctx, Kernel kern, dim3 grid, dim3 block,
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Resident blocks per SM of `kern` at (threads, smem), cached per device: the answer
-// depends only on the compiled kernel and the device, so it is queried once.
+// Resident blocks per SM of `kern` at (threads, smem), cached per device and kernel: the
+// answer depends only on the compiled kernel and the device, so it is queried once.
+// Kernels that cannot be resident at all report 0.
 template <typename Kernel>
 cudaError_t blocks_per_sm(const LaunchCtx& ctx, Kernel kern, int threads, size_t smem, int* out) {
-    constexpr int kDevices = 64, kSlots = 4;
+    constexpr int kDevices = 64, kSlots = 16;
     struct Entry {
+        const void* fn;
         int threads;
         size_t smem;
-        int value;
+        int value;  // -1: not cached
     };
     static std::mutex mu;
-    static Entry cache[kDevices][kSlots] = {};
+    static Entry cache[kDevices][kSlots];
+    static bool init = false;
+    const void* fn = reinterpret_cast<const void*>(kern);
     const int dev = ctx.device >= 0 && ctx.device < kDevices ? ctx.device : -1;
     if (dev >= 0) {
         std::lock_guard<std::mutex> lock(mu);
+        if (!init) {
+            for (auto& row : cache)
+                for (Entry& e : row) e = Entry{nullptr, 0, 0, -1};
+            init = true;
+        }
         for (const Entry& e : cache[dev])
-            if (e.value > 0 && e.threads == threads && e.smem == smem) {
+            if (e.value >= 0 && e.fn == fn && e.threads == threads && e.smem == smem) {
                 *out = e.value;
                 return cudaSuccess;
             }
@@ -61,12 +70,11 @@ cudaError_t blocks_per_sm(const LaunchCtx& ctx, Kernel kern, int threads, size_t
     int v = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, smem);
     if (err != cudaSuccess) return err;
-    if (v < 1) v = 1;
     if (dev >= 0) {
         std::lock_guard<std::mutex> lock(mu);
         for (Entry& e : cache[dev])
-            if (e.value == 0) {
-                e = Entry{threads, smem, v};
+            if (e.value < 0) {
+                e = Entry{fn, threads, smem, v};
                 break;
             }
     }

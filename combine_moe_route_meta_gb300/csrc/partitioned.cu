@@ -217,7 +217,7 @@ cudaError_t launch_units(const LaunchCtx& ctx, Kernel kern, const PartArgs& a, i
     cudaError_t err = blocks_per_sm(ctx, kern, kThreads, 0, &per_sm);
     if (err != cudaSuccess) return err;
     const int64_t need = std::max((a.n_units * 32 + kThreads - 1) / kThreads, (extra_threads + kThreads - 1) / kThreads);
-    const int64_t cap = int64_t(ctx.num_sms) * per_sm;
+    const int64_t cap = int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1);
     const int grid = int(std::max<int64_t>(1, std::min(need, cap)));
     return launch_pdl(ctx, kern, dim3(grid), dim3(kThreads), 0, a);
 }

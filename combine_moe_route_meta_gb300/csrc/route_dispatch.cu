@@ -12,9 +12,9 @@
 //     so the previous kernel's hidden_states and topk_ids are complete);
 //  2. for each of its K pairs (expert e_k, flattened index i_k) it needs only two counts
 //     over all T*K ids: #{valid ids < e_k} = seg_indptr[e_k] and #{j < i_k : id_j = e_k},
-//     the stable rank. All threads take both counts in one strided pass over the ids
-//     (register counters), reduce them with the hardware warp reduction and one
-//     shared-memory step;
+//     the stable rank. The ids are staged in shared memory in one round of loads; all
+//     threads then take both counts in one strided pass (register counters), reduce them
+//     with the hardware warp reduction and one shared-memory step;
 //  3. it writes its K entries of src2dst / reorder_topk_ids, and quantises and stores its
 //     row slices into the K destination rows (dispatch_slice.cuh).
 // Block T builds the full histogram and its exclusive scan and writes seg_indptr,
@@ -93,11 +93,13 @@ __device__ void fused_global_metadata(const FusedArgs& a, int* smem) {
     const int tid = threadIdx.x, lane = tid & 31, E = a.E;
     int* warp_sums = smem;        // [32]
     int* s_seg = smem + 32;       // [E + 1]
+    int* s_ids = s_seg + E + 1;   // [n_pairs]
     for (int e = tid; e < E; e += blockDim.x) s_seg[e] = 0;
+    stage_to_shared(a.ids, s_ids, a.n_pairs);
     __syncthreads();
     bool bad = false;
     for (int j = tid; j < a.n_pairs; j += blockDim.x) {
-        const int v = __ldg(a.ids + j);
+        const int v = s_ids[j];
         if (v >= 0 && v < E) atomicAdd(&s_seg[v], 1);
         else if (v != -1) bad = true;
     }
@@ -130,10 +132,10 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
         fused_global_metadata(a, reinterpret_cast<int*>(smem_raw));
         return;
     }
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     int64_t* s_row = reinterpret_cast<int64_t*>(smem_raw);         // [MOE_MAX_TOPK]
     int* s_part = reinterpret_cast<int*>(s_row + MOE_MAX_TOPK);     // [warps][2 * KMAX]
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    int* s_ids = s_part + nw * 2 * KMAX;                            // [n_pairs]
     const int t = blockIdx.x, H = a.H, K = a.K, E = a.E;
 
     // 1. this warp's first row slice, in flight during the counting
@@ -144,16 +146,18 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
     if (active) sl = load_slice(a.x + int64_t(t) * H + col);
 
     // 2. per pair k: less[k] = #{valid ids < e_k}, rank[k] = #{j < i_k : id_j == e_k}
+    stage_to_shared(a.ids, s_ids, a.n_pairs);
+    __syncthreads();
     const int base = t * K;
     int ek[KMAX], less[KMAX], rank[KMAX];
 #pragma unroll
     for (int k = 0; k < KMAX; k++) {
-        ek[k] = k < K ? __ldg(a.ids + base + k) : -2;
+        ek[k] = k < K ? s_ids[base + k] : -2;
         less[k] = 0;
         rank[k] = 0;
     }
     for (int j = tid; j < a.n_pairs; j += blockDim.x) {
-        const int v = __ldg(a.ids + j);
+        const int v = s_ids[j];
         const bool ok = v >= 0;
 #pragma unroll
         for (int k = 0; k < KMAX; k++) {
@@ -176,7 +180,7 @@ __global__ void route_dispatch_small_kernel(FusedArgs a) {
 
     // 3. this token's metadata entries and destination rows
     if (tid < K) {
-        const int k = tid, i = base + k, e = __ldg(a.ids + i);
+        const int k = tid, i = base + k, e = s_ids[i];
         int64_t row = -1;
         if (e >= 0 && e < E) {
             int seg_e = 0, r = 0;
@@ -212,8 +216,10 @@ cudaError_t launch_fused(const LaunchCtx& ctx, const FusedArgs& a) {
                          : route_dispatch_small_kernel<QUANT, MASKED, MOE_MAX_TOPK>;
     int threads = a.units_per_row * 32;
     threads = threads < 128 ? 128 : (threads > 512 ? 512 : threads);
-    const size_t token_smem = sizeof(int64_t) * MOE_MAX_TOPK + sizeof(int) * size_t(threads / 32) * 2 * MOE_MAX_TOPK;
-    const size_t meta_smem = sizeof(int) * (32 + size_t(a.E) + 1);
+    const int kmax = a.K <= 8 ? 8 : MOE_MAX_TOPK;
+    const size_t token_smem = sizeof(int64_t) * MOE_MAX_TOPK + sizeof(int) * size_t(threads / 32) * 2 * kmax +
+                              sizeof(int) * size_t(a.n_pairs);
+    const size_t meta_smem = sizeof(int) * (32 + size_t(a.E) + 1 + size_t(a.n_pairs));
     const size_t smem = token_smem > meta_smem ? token_smem : meta_smem;
     // blocks 0..T-1: one token each; block T: the per-expert outputs
     return launch_pdl(ctx, kern, dim3(a.T + 1), dim3(threads), smem, a);

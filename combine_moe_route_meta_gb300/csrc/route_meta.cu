@@ -279,33 +279,19 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_count_kernel(Rout
     }
 }
 
-// Several blocks, kernel 2: column sums of the table -> offsets and seg_indptr; final positions.
-// shared memory: part_pre[G][E] | part_tot[G][E] | tot[E] | pre[E] | seg[E+1] | warp_sums[32]
-__global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteArgs a) {
-    extern __shared__ int smem[];
-    pdl_launch_dependents();
-    pdl_wait();
-    const int E = a.E, B = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
-    const int G = min(kRouteThreads / E, kWarps);  // threads per column
-    int* part_pre = smem;
-    int* part_tot = part_pre + G * E;
-    int* tot = part_tot + G * E;
-    int* pre = tot + E;
-    int* seg = pre + E;
-    int* warp_sums = seg + E + 1;
+// Threads per table column in the column sums (blockDim == kRouteThreads).
+__host__ __device__ constexpr int table_cols_g(int E) {
+    return kRouteThreads / E < kWarps ? kRouteThreads / E : kWarps;
+}
 
-    // this thread's first pair (in-block rank and expert) is fetched before the table work
-    const int64_t i0 = int64_t(b) * kRouteThreads * a.R;
-    const int64_t i1 = min(a.n_pairs, i0 + int64_t(kRouteThreads) * a.R);
-    int d_first = -1, e_first = -1;
-    if (i0 + tid < i1) {
-        d_first = a.src2dst[i0 + tid];
-        e_first = read_id(a.ids, a.ids64, i0 + tid);
-    }
-
-    // every block reads the whole table: G threads per column, each a contiguous run of
-    // rows fetched kColBatch loads at a time
+// Column sums of the [B][E] table, read from L2: pre[e] = sum of rows < b (block b's
+// per-expert offsets), tot[e] = sum of all rows (the histogram). Every block reads the whole
+// table: G threads per column, each a contiguous run of rows fetched kColBatch loads at a
+// time. part_pre / part_tot: shared [G][E]. Ends with __syncthreads.
+__device__ void table_column_sums(const int32_t* table, int B, int b, int E, int* part_pre, int* part_tot,
+                                  int* pre, int* tot) {
     constexpr int kColBatch = 16;
+    const int tid = threadIdx.x, G = table_cols_g(E);
     const int rows_per = (B + G - 1) / G;
     const int col = tid % E, g = tid / E;
     if (tid < G * E) {
@@ -315,7 +301,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteAr
             int v[kColBatch];
 #pragma unroll
             for (int j = 0; j < kColBatch; j++)
-                v[j] = c0 + j < b1 ? __ldcg(a.table + size_t(c0 + j) * E + col) : 0;
+                v[j] = c0 + j < b1 ? __ldcg(table + size_t(c0 + j) * E + col) : 0;
 #pragma unroll
             for (int j = 0; j < kColBatch; j++) {
                 q += v[j];
@@ -336,6 +322,33 @@ __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteAr
         tot[tid] = q;
     }
     __syncthreads();
+}
+
+// Several blocks, kernel 2: column sums of the table -> offsets and seg_indptr; final positions.
+// shared memory: part_pre[G][E] | part_tot[G][E] | tot[E] | pre[E] | seg[E+1] | warp_sums[32]
+__global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteArgs a) {
+    extern __shared__ int smem[];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int E = a.E, B = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
+    const int G = table_cols_g(E);
+    int* part_pre = smem;
+    int* part_tot = part_pre + G * E;
+    int* tot = part_tot + G * E;
+    int* pre = tot + E;
+    int* seg = pre + E;
+    int* warp_sums = seg + E + 1;
+
+    // this thread's first pair (in-block rank and expert) is fetched before the table work
+    const int64_t i0 = int64_t(b) * kRouteThreads * a.R;
+    const int64_t i1 = min(a.n_pairs, i0 + int64_t(kRouteThreads) * a.R);
+    int d_first = -1, e_first = -1;
+    if (i0 + tid < i1) {
+        d_first = a.src2dst[i0 + tid];
+        e_first = read_id(a.ids, a.ids64, i0 + tid);
+    }
+
+    table_column_sums(a.table, B, b, E, part_pre, part_tot, pre, tot);
     finish_histogram(tot, seg, warp_sums, E, a.P, a.M, a.A, a.seg_indptr, a.masked_m, a.partition_counts,
                      a.reorder, a.status, b == 0);
 
@@ -370,7 +383,7 @@ cudaError_t launch_rmax(const LaunchCtx& ctx, const RoutePlan& plan, const Route
     cudaError_t err = launch_pdl(ctx, k1, dim3(plan.blocks), dim3(kRouteThreads), smem, a);
     if (err != cudaSuccess) return err;
     // kernel 2's launch overlaps kernel 1's tail; griddepcontrol.wait orders its reads
-    const int G = std::min(kRouteThreads / E, kWarps);
+    const int G = table_cols_g(E);
     const size_t smem2 = sizeof(int) * (size_t(2 * G) * E + 3 * size_t(E) + 1 + 32);
     return launch_pdl(ctx, route_meta_place_kernel, dim3(plan.blocks), dim3(kRouteThreads), smem2, a);
 }

@@ -96,7 +96,8 @@ const char *moe_status_string(moe_status_t status);
  * Bytes of scratch that moe_route_meta needs for num_tokens x topk pairs and
  * num_experts experts (0 when one thread block handles all pairs). The workspace
  * must be zero-filled once when it is allocated; every call that completes leaves
- * it ready for the next call. Returns 0 for arguments moe_route_meta would reject.
+ * it ready for the next call. Calls that share a workspace must not overlap on the GPU.
+ * Returns 0 for arguments moe_route_meta would reject.
  */
 size_t moe_route_meta_workspace_size(int64_t num_tokens, int topk, int num_experts);
 

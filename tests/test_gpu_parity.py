@@ -99,6 +99,29 @@ def test_large_route_meta_many_rounds():
     assert np.array_equal(gm.reorder_topk_ids[: om.num_valid].cpu().numpy(), om.reorder_topk_ids)
 
 
+@pytest.mark.parametrize("T,K,E,routing", [
+    (400000, 8, 256, "uniform"),  # 196 blocks of 16 rounds: more than can be resident -> two launches
+    (20000, 8, 1024, "zipf"),     # 79 blocks of 2 rounds, E = 1024: the largest shared-memory footprint
+    (9000, 1, 7, "uniform"),      # 9 blocks, odd E smaller than a warp
+])
+def test_multi_block_route_meta_paths(T, K, E, routing):
+    """Multi-block metadata in full: the single cooperative launch and, past the number of
+    resident blocks, the two-launch fallback; the workspace is reused across calls."""
+    w = make_case(T, 16, E, K, seed=T + E, routing=routing, invalid_rate=0.03)
+    _, ids, _ = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, w.E)
+    m = moe()
+    d = m.MoEDispatcher(w.T, w.H, w.K, w.E)
+    for _ in range(2):
+        d.route(ids)
+        torch.cuda.synchronize()
+        assert np.array_equal(d.src2dst.cpu().numpy(), om.src2dst)
+        assert np.array_equal(d.seg_indptr.cpu().numpy(), om.seg_indptr)
+        assert np.array_equal(d.reorder_topk_ids[: om.num_valid].cpu().numpy(), om.reorder_topk_ids)
+        assert np.array_equal(d.masked_m.cpu().numpy(), om.masked_m)
+    d.check()
+
+
 # --- degenerate inputs ---------------------------------------------------------------
 
 def test_empty_batch():
@@ -187,14 +210,20 @@ def test_repeated_calls_reuse_workspace():
     d.check()
 
 
-def test_dispatcher_graph_capture_replays_correctly():
-    """route + dispatch + combine captured in one CUDA graph and replayed."""
+@pytest.mark.parametrize("case", ["decode", "normal_4096"])
+def test_dispatcher_graph_capture_replays_correctly(case):
+    """route + dispatch + combine captured in one CUDA graph and replayed (decode: one-block
+    metadata; normal_4096: the cooperative multi-block metadata and the bulk dispatch)."""
     m = moe()
-    w = make_workload("decode")
+    if case == "decode":
+        w = make_workload("decode")
+    else:
+        w = make_case(4096, 1024, 256, 8, seed=21, quant="fp8g128", routing="zipf", invalid_rate=0.02)
     x, ids, wt = to_dev(w)
-    d = m.MoEDispatcher(w.T, w.H, w.K, w.E, mode="masked", quant="fp8g128", num_partitions=w.P,
+    d = m.MoEDispatcher(w.T, w.H, w.K, w.E, mode=w.mode, quant=w.quant, num_partitions=w.P,
                         max_tokens_per_expert=w.M)
-    eo = torch.randn((w.E * w.M, w.H), dtype=torch.bfloat16, device="cuda")
+    eo_rows = w.E * w.M if w.mode == "masked" else w.T * w.K
+    eo = torch.randn((eo_rows, w.H), dtype=torch.bfloat16, device="cuda")
     d.out_q.zero_()            # slots past masked_m are never written: start both runs from zeros
     d.out.zero_()
     s = torch.cuda.Stream()
