@@ -84,6 +84,7 @@ def _load():
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int32, f32, P, P, P, P]),
             "oracle_combine_partitioned": (None, [P, i64, i64, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
                                                   ctypes.c_int, P]),
+            "oracle_nvfp4_sf_interleave": (None, [P, i64, ctypes.c_int, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -328,3 +329,18 @@ def quant_fp8_ue8m0_row(x_row: np.ndarray):
     e = np.empty(H // 128, np.uint8)
     _load().oracle_quant_fp8_g128_ue8m0_row(_ptr(x_row), H, _ptr(q), _ptr(e))
     return q, e
+
+
+# ---------------------------------------------------------------------------
+# CUTLASS consumer format: interleaved NVFP4 block scales
+# ---------------------------------------------------------------------------
+
+def nvfp4_sf_interleave(sf: np.ndarray) -> np.ndarray:
+    """nvfp4_block_scale_interleave of a [rows, cols] uint8 block-scale matrix: 1-D uint8 of
+    round_up(rows, 128) * round_up(cols, 4) bytes in the 128 x 4 tile layout, zero padding."""
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    rows, cols = sf.shape
+    n = (rows + 127) // 128 * 128 * ((cols + 3) // 4 * 4)
+    out = np.empty(n, np.uint8)
+    _load().oracle_nvfp4_sf_interleave(_ptr(sf), rows, cols, _ptr(out))
+    return out

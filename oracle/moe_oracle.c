@@ -28,7 +28,8 @@
  *    num_max_dispatch_tokens_per_rank, use_nvfp4 with x_global_scale).
  *  - "sglang token_dispatcher/flashinfer.py" page: FlashinferDispatcher.__init__
  *    (dispatch payload bytes per token) and dispatch (fp4_quantize with
- *    input_global_scale, non-swizzled e4m3 block scales).
+ *    input_global_scale, non-swizzled e4m3 block scales; nvfp4_block_scale_interleave
+ *    of the received scales for the CUTLASS MoE).
  *
  * Readings where the pages are silent (the metadata routine's body, the exact
  * quantisation arithmetic, the masked slot order) are listed beside each function.
@@ -623,5 +624,31 @@ void oracle_quant_fp8_g128_ue8m0_row(const uint16_t *x, int H, uint8_t *q, uint8
         float s2 = (float)ldexp(1.0, k);
         for (int j = 0; j < 128; j++) q[(size_t)g * 128 + j] = oracle_e4m3_from_float(bf16_to_float(xg[j]) / s2);
         scale_exp[g] = (uint8_t)(k + 127);
+    }
+}
+
+/*
+ * nvfp4_block_scale_interleave(x_sf) (flashinfer.py page, FlashinferDispatcher.dispatch, applied
+ * to the received block scales, flattened to [rows, cols], before the CUTLASS MoE).
+ * Reading (the page names the call only): the scale-factor layout of the block-scaled tensor-core
+ * MMA as publicly documented for NVFP4 -- the [rows, cols] byte matrix is padded with zeros to
+ * rows a multiple of 128 and cols a multiple of 4, cut into 128 x 4 tiles stored one after the
+ * other in row-tile-major order (512 bytes each), and inside a tile the scale of tile row i
+ * (0..127) and tile column c (0..3) sits at byte (i % 32) * 16 + (i / 32) * 4 + c: each
+ * 16-byte line holds rows j, j+32, j+64, j+96 for the tile's 4 columns.
+ * out: ((rows + 127) / 128 * 128) * ((cols + 3) / 4 * 4) bytes.
+ */
+void oracle_nvfp4_sf_interleave(const uint8_t *sf, int64_t rows, int cols, uint8_t *out)
+{
+    const int64_t row_tiles = (rows + 127) / 128;
+    const int64_t col_tiles = (cols + 3) / 4;
+    memset(out, 0, (size_t)(row_tiles * 128 * col_tiles * 4));
+    for (int64_t r = 0; r < rows; r++) {
+        for (int c = 0; c < cols; c++) {
+            int64_t tile = (r / 128) * col_tiles + c / 4;
+            int64_t i = r % 128;
+            int64_t at = tile * 512 + (i % 32) * 16 + (i / 32) * 4 + c % 4;
+            out[at] = sf[r * cols + c];
+        }
     }
 }

@@ -83,3 +83,51 @@ def test_fp8_passthrough_rows_are_byte_copies(mode):
         assert np.array_equal(rows[r], codes[i // w.K])
         hit[r] = True
     assert (rows[~hit] == 0xC3).all()
+
+
+# --- interleaved NVFP4 block scales (nvfp4_block_scale_interleave) ---------------------------
+
+def _interleave_by_reshape(sf: np.ndarray) -> np.ndarray:
+    """The same layout stated as array reshapes: rows r = 128*rt + 32*i + j, columns
+    c = 4*ct + cc; the tile (rt, ct) is stored as [j][i][cc]."""
+    rows, cols = sf.shape
+    Rp, Cp = (rows + 127) // 128 * 128, (cols + 3) // 4 * 4
+    pad = np.zeros((Rp, Cp), np.uint8)
+    pad[:rows, :cols] = sf
+    t = pad.reshape(Rp // 128, 4, 32, Cp // 4, 4)       # rt, i, j, ct, cc
+    return t.transpose(0, 3, 2, 1, 4).reshape(-1)        # rt, ct, j, i, cc
+
+
+@pytest.mark.parametrize("rows,cols", [(128, 4), (256, 448), (77, 448), (300, 6), (1, 1), (1024, 256)])
+def test_sf_interleave_matches_reshape_definition(rows, cols):
+    sf = np.random.default_rng(rows * 7 + cols).integers(0, 256, (rows, cols), dtype=np.uint8)
+    got = oracle.nvfp4_sf_interleave(sf)
+    assert got.shape == ((rows + 127) // 128 * 128 * ((cols + 3) // 4 * 4),)
+    assert np.array_equal(got, _interleave_by_reshape(sf))
+
+
+def test_sf_interleave_first_lines_and_padding():
+    """Each 16-byte line holds rows j, j+32, j+64, j+96 of the tile's 4 columns; the next
+    4 columns start a new 512-byte tile; padded rows and columns are zero."""
+    rows, cols = 100, 6
+    sf = (np.arange(rows * cols) % 251 + 1).astype(np.uint8).reshape(rows, cols)  # no zeros
+    got = oracle.nvfp4_sf_interleave(sf)
+    assert list(got[0:4]) == list(sf[0, 0:4])
+    assert list(got[4:8]) == list(sf[32, 0:4])
+    assert list(got[8:12]) == list(sf[64, 0:4])
+    assert list(got[12:16]) == list(sf[96, 0:4])
+    assert list(got[16:20]) == list(sf[1, 0:4])
+    assert list(got[512:514]) == list(sf[0, 4:6]) and list(got[514:516]) == [0, 0]   # cols 6, 7 pad
+    assert list(got[12 + 16 * 4: 16 + 16 * 4]) == [0, 0, 0, 0]                         # row 100 pad
+    assert int(np.count_nonzero(got)) == rows * cols
+
+
+def test_sf_interleave_is_a_permutation_of_full_tiles():
+    """On whole tiles every source byte lands in exactly one place: tracking a 16-bit index
+    through the interleave as two byte planes recovers a permutation."""
+    rows, cols = 256, 8
+    idx = np.arange(rows * cols, dtype=np.uint16).reshape(rows, cols)
+    lo = oracle.nvfp4_sf_interleave((idx & 0xFF).astype(np.uint8))
+    hi = oracle.nvfp4_sf_interleave((idx >> 8).astype(np.uint8))
+    where = lo.astype(np.int64) | (hi.astype(np.int64) << 8)
+    assert np.array_equal(np.sort(where), np.arange(rows * cols))
