@@ -48,7 +48,8 @@ QUANTS = {"none": MOE_QUANT_NONE, "fp8g128": MOE_QUANT_FP8_G128, "nvfp4b16": MOE
 MOE_QUANT_FP8_PASSTHROUGH = 4
 MOE_SCALES_ROW_MAJOR = 0
 MOE_SCALES_COL_MAJOR = 1
-SCALE_LAYOUTS = {"row": MOE_SCALES_ROW_MAJOR, "col": MOE_SCALES_COL_MAJOR}
+MOE_SCALES_SWIZZLED_128X4 = 2
+SCALE_LAYOUTS = {"row": MOE_SCALES_ROW_MAJOR, "col": MOE_SCALES_COL_MAJOR, "swizzled": MOE_SCALES_SWIZZLED_128X4}
 
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_TOPK = 16
@@ -76,6 +77,8 @@ _SIGNATURES = {
     "moe_dispatch_partitioned": (_int, [_int, _P, _i64, _i64, _int, _P, _P, _int, _int, _int, _i32, _f32, _P, _P,
                                         _P, _P, _P, _P]),
     "moe_combine_partitioned": (_int, [_P, _i64, _i64, _int, _P, _int, _int, _int, _P, _P, _P]),
+    "moe_dispatch_partitioned_ex": (_int, [_int, _int, _P, _i64, _i64, _int, _P, _P, _int, _int, _int, _i32, _f32,
+                                           _P, _P, _P, _P, _P, _P]),
 }
 _lib_handle = None
 
@@ -299,6 +302,26 @@ def moe_dispatch_partitioned(quant: str, hidden_states: torch.Tensor, topk_ids: 
         num_partitions, int(invalid_expert_id), float(input_global_scale), _ptr(recv_x), _ptr(recv_scales),
         _ptr(recv_topk_ids), _ptr(recv_topk_weights), _ptr(dev_status), _stream(stream))
     _check(st, "moe_dispatch_partitioned")
+
+
+def moe_dispatch_partitioned_ex(quant: str, scale_layout: str, hidden_states: torch.Tensor, topk_ids: torch.Tensor,
+                                topk_weights: torch.Tensor, num_experts: int, num_partitions: int,
+                                recv_x: torch.Tensor, recv_scales: Optional[torch.Tensor], recv_topk_ids: torch.Tensor,
+                                recv_topk_weights: torch.Tensor, dev_status: torch.Tensor, invalid_expert_id: int = -1,
+                                input_global_scale: float = 0.0, stream=None) -> None:
+    T, H = hidden_states.shape
+    K = topk_ids.shape[1]
+    S = recv_topk_ids.shape[1]
+    st = load_library().moe_dispatch_partitioned_ex(
+        QUANTS[quant], SCALE_LAYOUTS[scale_layout], _ptr(hidden_states), T, S, H, _ptr(topk_ids), _ptr(topk_weights),
+        K, num_experts, num_partitions, int(invalid_expert_id), float(input_global_scale), _ptr(recv_x),
+        _ptr(recv_scales), _ptr(recv_topk_ids), _ptr(recv_topk_weights), _ptr(dev_status), _stream(stream))
+    _check(st, "moe_dispatch_partitioned_ex")
+
+
+def swizzled_scale_bytes(rows: int, hidden: int) -> int:
+    """Bytes of a MOE_SCALES_SWIZZLED_128X4 NVFP4 scale buffer for `rows` destination rows."""
+    return (rows + 127) // 128 * 128 * (hidden // 16)
 
 
 def moe_combine_partitioned(partial: torch.Tensor, topk_ids: torch.Tensor, num_experts: int, num_partitions: int,

@@ -312,7 +312,9 @@ BulkGeom bulk_geometry(int quant, const DispatchArgs& a) {
         default: g.q_bytes = uint32_t(H / 2); g.s_bytes = uint32_t(H / 16); break;
     }
     const bool aligned16 = (reinterpret_cast<uintptr_t>(a.out_s) & 15) == 0;
-    if (g.q_bytes % 16 || g.s_bytes % 16 || a.L.col_major || (quant != MOE_QUANT_NONE && !aligned16)) return g;
+    if (g.q_bytes % 16 || g.s_bytes % 16 || a.L.kind != MOE_SCALES_ROW_MAJOR ||
+        (quant != MOE_QUANT_NONE && !aligned16))
+        return g;
     const uint32_t seg_bytes = uint32_t(sizeof(int)) * uint32_t(a.E);
     const int stages = quant == MOE_QUANT_NONE ? 4 : 3;
     g.in_off = kBulkHeader;
@@ -404,6 +406,28 @@ cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t 
     return cudaGetLastError();
 }
 
+// Zeros of the padding rows [R, roundup(R, 128)) of a 128 x 4 swizzled scale matrix with C
+// columns (C % 4 == 0): one thread per 4-byte word (row, tile column).
+__global__ void sf_swizzle_pad_kernel(uint8_t* sf, int64_t R, int C, int64_t n_words) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (j >= n_words) return;
+    const int C4 = C / 4;
+    const int64_t r = R + j / C4;
+    const int ct = int(j - (j / C4) * C4);
+    *reinterpret_cast<uint32_t*>(sf + swizzled_128x4_index(r, 4 * ct, C)) = 0u;
+}
+
+cudaError_t launch_sf_swizzle_pad(const LaunchCtx& ctx, uint8_t* sf, int64_t R, int C) {
+    const int64_t Rp = (R + 127) / 128 * 128;
+    const int64_t n_words = (Rp - R) * (C / 4);
+    if (n_words == 0) return cudaSuccess;
+    const int threads = 256;
+    return launch_pdl(ctx, sf_swizzle_pad_kernel, dim3(unsigned((n_words + threads - 1) / threads)), dim3(threads),
+                      0, sf, R, C, n_words);
+}
+
 cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uint16_t* x, int64_t T,
                             int H, const int32_t* topk_ids, int K, int E, int M,
                             const int32_t* src2dst, const int64_t* seg_indptr, float global_scale,
@@ -427,9 +451,14 @@ cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uin
     a.n_units = T * a.units_per_row;
     a.max_row = out_rows > 0 ? out_rows : T * K;
     const bool masked = mode == MOE_MODE_MASKED;
-    a.L.col_major = scale_layout;
+    a.L.kind = scale_layout;
     a.L.M = masked ? M : 0;
     a.L.rows_al = ((masked ? int64_t(M) : a.max_row) + 3) / 4 * 4;
+    if (scale_layout == MOE_SCALES_SWIZZLED_128X4) {
+        cudaError_t err = launch_sf_swizzle_pad(ctx, static_cast<uint8_t*>(out_scales),
+                                                masked ? int64_t(E) * M : a.max_row, H / 16);
+        if (err != cudaSuccess) return err;
+    }
     switch (quant) {
         case MOE_QUANT_NONE:
             return masked ? launch_variant<MOE_QUANT_NONE, true>(ctx, a)

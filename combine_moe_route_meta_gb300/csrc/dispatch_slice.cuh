@@ -17,17 +17,29 @@
 
 namespace moe {
 
-// Where the scales of a destination row go (MOE_SCALES_ROW_MAJOR / MOE_SCALES_COL_MAJOR).
+// Where the scales of a destination row go (moe_scale_layout_t).
 struct ScaleLayout {
-    int col_major;    // 0: [rows, G] row-major; 1: MN-major with rows padded to a multiple of 4
+    int kind;         // MOE_SCALES_ROW_MAJOR: [rows, G]; MOE_SCALES_COL_MAJOR: MN-major with rows
+                      // padded to a multiple of 4; MOE_SCALES_SWIZZLED_128X4: 128 x 4 tiles
     int64_t rows_al;  // column-major: padded rows (normal layout) or padded slots M (masked)
     int M;            // masked layout: slots per expert; 0 for the contiguous layout
 };
 
+// Byte offset of scale column g (of G, a multiple of 4) of row r in the 128 x 4 tile layout
+// of the block-scaled MMA (nvfp4_block_scale_interleave): tiles of 128 rows x 4 columns,
+// 512 bytes each, in row-tile-major order; inside a tile, row i and column c at
+// (i % 32) * 16 + (i / 32) * 4 + c.
+__host__ __device__ __forceinline__ int64_t swizzled_128x4_index(int64_t r, int g, int G) {
+    const int64_t tile = (r >> 7) * (G >> 2) + (g >> 2);
+    const int i = int(r & 127);
+    return tile * 512 + (i & 31) * 16 + (i >> 5) * 4 + (g & 3);
+}
+
 // Element index of group g's scale for destination `row`: fp32 elements, or bytes when
-// `packed4` (UE8M0: four groups per int32 word, little-endian).
+// `packed4` (UE8M0: four groups per int32 word, little-endian) or for the swizzled layout.
 __device__ __forceinline__ int64_t scale_index(const ScaleLayout& L, int64_t row, int g, int G, bool packed4) {
-    if (!L.col_major) return row * G + g;
+    if (L.kind == MOE_SCALES_ROW_MAJOR) return row * G + g;
+    if (L.kind == MOE_SCALES_SWIZZLED_128X4) return swizzled_128x4_index(row, g, G);
     int64_t e = 0, r = row;
     if (L.M > 0) {
         e = row / L.M;
@@ -124,7 +136,7 @@ __device__ __forceinline__ LaneCodes quantise16(const LaneSlice& s, float g) {
 template <int QUANT>
 __device__ __forceinline__ void quantise_store(const LaneSlice& s, bool active, int lane, int col, int H,
                                                int K, int64_t my_row, float g, void* out_q,
-                                               void* out_s, const ScaleLayout& L = ScaleLayout{0, 0, 0}) {
+                                               void* out_s, const ScaleLayout& L = ScaleLayout{MOE_SCALES_ROW_MAJOR, 0, 0}) {
     if constexpr (QUANT == MOE_QUANT_NONE) {
         uint16_t* out = static_cast<uint16_t*>(out_q);
         for (int k = 0; k < K; k++) {
@@ -152,7 +164,7 @@ __device__ __forceinline__ void quantise_store(const LaneSlice& s, bool active, 
                     static_cast<uint8_t*>(out_s)[scale_index(L, row, col / 128, groups, true)] = uint8_t(c.scale);
             } else {
                 st_v2(out + row * (H / 2) + col / 2, make_uint2(c.q.x, c.q.y));
-                static_cast<uint8_t*>(out_s)[row * (H / 16) + col / 16] = uint8_t(c.scale);
+                static_cast<uint8_t*>(out_s)[scale_index(L, row, col / 16, H / 16, true)] = uint8_t(c.scale);
             }
         }
     }

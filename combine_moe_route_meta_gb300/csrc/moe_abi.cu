@@ -141,8 +141,11 @@ static moe_status_t dispatch_impl(moe_mode_t mode, moe_quant_t quant, moe_scale_
                                   moe_stream_t stream) {
     if (mode != MOE_MODE_NORMAL && mode != MOE_MODE_MASKED) return MOE_ERR_INVALID_ARG;
     if (!valid_quant(quant)) return MOE_ERR_INVALID_ARG;
-    if (layout != MOE_SCALES_ROW_MAJOR && layout != MOE_SCALES_COL_MAJOR) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_SCALES_ROW_MAJOR && layout != MOE_SCALES_COL_MAJOR && layout != MOE_SCALES_SWIZZLED_128X4)
+        return MOE_ERR_INVALID_ARG;
     if (layout == MOE_SCALES_COL_MAJOR && !is_fp8(quant)) return MOE_ERR_INVALID_ARG;
+    if (layout == MOE_SCALES_SWIZZLED_128X4 && (quant != MOE_QUANT_NVFP4_B16 || hidden % 64 != 0))
+        return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_shape(num_tokens, topk, num_experts);
     if (st != MOE_OK) return st;
     if (hidden <= 0 || hidden % 16 != 0) return MOE_ERR_INVALID_ARG;
@@ -160,7 +163,8 @@ static moe_status_t dispatch_impl(moe_mode_t mode, moe_quant_t quant, moe_scale_
     if (!aligned(hidden_states, 16) || !aligned(out_q, 16) || !aligned(src2dst, 4) ||
         !aligned(topk_ids, 4) || !aligned(seg_indptr, 8) || !aligned(dev_status, 4))
         return MOE_ERR_INVALID_ARG;
-    if (quant == MOE_QUANT_FP8_G128 && !aligned(out_scales, 4)) return MOE_ERR_INVALID_ARG;
+    if ((quant == MOE_QUANT_FP8_G128 || layout == MOE_SCALES_SWIZZLED_128X4) && !aligned(out_scales, 4))
+        return MOE_ERR_INVALID_ARG;
     moe::LaunchCtx ctx;
     st = make_ctx(stream, &ctx);
     if (st != MOE_OK) return st;
@@ -319,13 +323,19 @@ static moe_status_t check_partitioned(int64_t T, int64_t S, int H, int K, int E,
     return MOE_OK;
 }
 
-moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t* hidden_states, int64_t num_tokens,
-                                      int64_t num_slots, int hidden, const int32_t* topk_ids,
-                                      const float* topk_weights, int topk, int num_experts, int num_partitions,
-                                      int32_t invalid_expert_id, float input_global_scale, void* recv_x,
-                                      uint8_t* recv_scales, int32_t* recv_topk_ids, float* recv_topk_weights,
-                                      int32_t* dev_status, moe_stream_t stream) {
+static moe_status_t dispatch_partitioned_impl(moe_quant_t quant, moe_scale_layout_t layout,
+                                              const uint16_t* hidden_states, int64_t num_tokens,
+                                              int64_t num_slots, int hidden, const int32_t* topk_ids,
+                                              const float* topk_weights, int topk, int num_experts,
+                                              int num_partitions, int32_t invalid_expert_id,
+                                              float input_global_scale, void* recv_x, uint8_t* recv_scales,
+                                              int32_t* recv_topk_ids, float* recv_topk_weights,
+                                              int32_t* dev_status, moe_stream_t stream) {
     if (quant != MOE_QUANT_NONE && quant != MOE_QUANT_NVFP4_B16) return MOE_ERR_INVALID_ARG;
+    if (layout != MOE_SCALES_ROW_MAJOR && layout != MOE_SCALES_SWIZZLED_128X4) return MOE_ERR_INVALID_ARG;
+    if (layout == MOE_SCALES_SWIZZLED_128X4 &&
+        (quant != MOE_QUANT_NVFP4_B16 || hidden % 64 != 0 || !aligned(recv_scales, 4)))
+        return MOE_ERR_INVALID_ARG;
     moe_status_t st = check_partitioned(num_tokens, num_slots, hidden, topk, num_experts, num_partitions);
     if (st != MOE_OK) return st;
     if (!dev_status) return MOE_ERR_INVALID_ARG;
@@ -342,7 +352,32 @@ moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t* hidden_
     return from_cuda(moe::launch_dispatch_partitioned(ctx, int(quant), hidden_states, num_tokens, num_slots, hidden,
                                                       topk_ids, topk_weights, topk, num_experts, num_partitions,
                                                       invalid_expert_id, input_global_scale, recv_x, recv_scales,
-                                                      recv_topk_ids, recv_topk_weights, dev_status));
+                                                      recv_topk_ids, recv_topk_weights, dev_status, int(layout)));
+}
+
+moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t* hidden_states, int64_t num_tokens,
+                                      int64_t num_slots, int hidden, const int32_t* topk_ids,
+                                      const float* topk_weights, int topk, int num_experts, int num_partitions,
+                                      int32_t invalid_expert_id, float input_global_scale, void* recv_x,
+                                      uint8_t* recv_scales, int32_t* recv_topk_ids, float* recv_topk_weights,
+                                      int32_t* dev_status, moe_stream_t stream) {
+    return dispatch_partitioned_impl(quant, MOE_SCALES_ROW_MAJOR, hidden_states, num_tokens, num_slots, hidden,
+                                     topk_ids, topk_weights, topk, num_experts, num_partitions, invalid_expert_id,
+                                     input_global_scale, recv_x, recv_scales, recv_topk_ids, recv_topk_weights,
+                                     dev_status, stream);
+}
+
+moe_status_t moe_dispatch_partitioned_ex(moe_quant_t quant, moe_scale_layout_t scale_layout,
+                                         const uint16_t* hidden_states, int64_t num_tokens, int64_t num_slots,
+                                         int hidden, const int32_t* topk_ids, const float* topk_weights, int topk,
+                                         int num_experts, int num_partitions, int32_t invalid_expert_id,
+                                         float input_global_scale, void* recv_x, uint8_t* recv_scales,
+                                         int32_t* recv_topk_ids, float* recv_topk_weights, int32_t* dev_status,
+                                         moe_stream_t stream) {
+    return dispatch_partitioned_impl(quant, scale_layout, hidden_states, num_tokens, num_slots, hidden, topk_ids,
+                                     topk_weights, topk, num_experts, num_partitions, invalid_expert_id,
+                                     input_global_scale, recv_x, recv_scales, recv_topk_ids, recv_topk_weights,
+                                     dev_status, stream);
 }
 
 moe_status_t moe_combine_partitioned(const uint16_t* partial, int64_t num_tokens, int64_t num_slots, int hidden,

@@ -120,6 +120,10 @@ cudaError_t launch_route_dispatch_small(const LaunchCtx& ctx, int mode, int quan
                                         int32_t* partition_counts, void* out_q, void* out_scales,
                                         int32_t* dev_status);
 
+// Zeros of the padding rows [R, roundup(R, 128)) of a 128 x 4 swizzled NVFP4 scale matrix
+// with C columns (C % 4 == 0; sf 4-byte aligned). dispatch.cu.
+cudaError_t launch_sf_swizzle_pad(const LaunchCtx& ctx, uint8_t* sf, int64_t R, int C);
+
 // Per-partition layout and the FlashInfer all-to-all layout (partitioned.cu).
 constexpr int kMaxPartitionsA2A = 32;
 cudaError_t launch_dispatch_layout(const LaunchCtx& ctx, const int32_t* ids, int64_t T, int K, int E, int P,
@@ -128,7 +132,8 @@ cudaError_t launch_dispatch_layout(const LaunchCtx& ctx, const int32_t* ids, int
 cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const uint16_t* x, int64_t T, int64_t S,
                                         int H, const int32_t* ids, const float* w, int K, int E, int P,
                                         int32_t invalid_id, float g, void* recv_x, uint8_t* recv_sf,
-                                        int32_t* recv_ids, float* recv_w, int32_t* dev_status);
+                                        int32_t* recv_ids, float* recv_w, int32_t* dev_status,
+                                        int scale_layout = 0);
 cudaError_t launch_combine_partitioned(const LaunchCtx& ctx, const uint16_t* partial, int64_t T, int64_t S, int H,
                                        const int32_t* ids, int K, int E, int P, uint16_t* out, int32_t* dev_status);
 

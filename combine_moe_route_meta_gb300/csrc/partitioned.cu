@@ -94,6 +94,7 @@ struct PartArgs {
     int32_t* status;
     int units_per_row;
     int64_t n_units;
+    ScaleLayout L;  // of recv_sf: row-major [P*S, H/16] or 128 x 4 swizzled over the P*S rows
 };
 
 // lane p: whether token t sends to partition p; all lanes return the same K ids in e_out
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_partitioned_kernel(PartArgs
             }
         }
         if constexpr (QUANT == MOE_QUANT_NVFP4_B16)
-            quantise_store<QUANT>(sl, active, lane, col, H, a.P, my_row, a.g, a.recv_x, a.recv_sf);
+            quantise_store<QUANT>(sl, active, lane, col, H, a.P, my_row, a.g, a.recv_x, a.recv_sf, a.L);
         else
             quantise_store<QUANT>(sl, active, lane, col, H, a.P, my_row, a.g, a.recv_x, nullptr);
     }
@@ -240,7 +241,7 @@ cudaError_t launch_dispatch_layout(const LaunchCtx& ctx, const int32_t* ids, int
 cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const uint16_t* x, int64_t T, int64_t S,
                                         int H, const int32_t* ids, const float* w, int K, int E, int P,
                                         int32_t invalid_id, float g, void* recv_x, uint8_t* recv_sf,
-                                        int32_t* recv_ids, float* recv_w, int32_t* dev_status) {
+                                        int32_t* recv_ids, float* recv_w, int32_t* dev_status, int scale_layout) {
     PartArgs a{};
     a.x = x;
     a.ids = ids;
@@ -261,6 +262,11 @@ cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const u
     a.status = dev_status;
     a.units_per_row = (H + kSlice - 1) / kSlice;
     a.n_units = T * a.units_per_row;
+    a.L = ScaleLayout{scale_layout, 0, 0};
+    if (quant == MOE_QUANT_NVFP4_B16 && scale_layout == MOE_SCALES_SWIZZLED_128X4) {
+        cudaError_t err = launch_sf_swizzle_pad(ctx, recv_sf, int64_t(P) * S, H / 16);
+        if (err != cudaSuccess) return err;
+    }
     const int64_t pad = (S - T) * P * K;
     if (a.n_units == 0 && pad == 0) return cudaSuccess;
     if (quant == MOE_QUANT_NVFP4_B16) return launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NVFP4_B16>, a, pad);

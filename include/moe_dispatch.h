@@ -73,13 +73,22 @@ typedef enum {
                                     per-tensor FP8): rows of H bytes are copied, no scales   */
 } moe_quant_t;
 
-/* Layout of the FP8 scale arrays (moe_dispatch_ex). */
+/* Layout of the scale arrays (moe_dispatch_ex, moe_dispatch_partitioned_ex). */
 typedef enum {
     MOE_SCALES_ROW_MAJOR = 0,  /* [rows, G]: group g of row r at r*G + g                      */
-    MOE_SCALES_COL_MAJOR = 1   /* MN-major, TMA-aligned: group g of row r at g*R4 + r with R4 =
-                                  rows rounded up to a multiple of 4 (per expert [E, G, R4] in
-                                  the masked layout, R4 from M); UE8M0 bytes: int32 word
-                                  (r, g/4) at (g/4)*R4 + r, byte g%4 of the word              */
+    MOE_SCALES_COL_MAJOR = 1,  /* FP8 only. MN-major, TMA-aligned: group g of row r at g*R4 + r
+                                  with R4 = rows rounded up to a multiple of 4 (per expert
+                                  [E, G, R4] in the masked layout, R4 from M); UE8M0 bytes:
+                                  int32 word (r, g/4) at (g/4)*R4 + r, byte g%4 of the word   */
+    MOE_SCALES_SWIZZLED_128X4 = 2 /* NVFP4 only, H % 64 == 0. The e4m3 block scales of all R
+                                  destination rows as one [R, C] matrix (C = H/16) in the 128 x 4
+                                  tile layout of the block-scaled MMA, as nvfp4_block_scale_interleave
+                                  produces it for the CUTLASS MoE (flashinfer.py page,
+                                  FlashinferDispatcher.dispatch): scale (r, c) at byte
+                                  ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4.
+                                  R = out_rows (normal), E*M (masked) or P*num_slots (partitioned);
+                                  the buffer holds roundup(R, 128)*C bytes and the padding rows
+                                  R..roundup(R, 128)-1 are written as zeros. 4-byte aligned.  */
 } moe_scale_layout_t;
 
 #define MOE_MAX_EXPERTS 1024   /* E <= 1024                                  */
@@ -258,6 +267,8 @@ moe_status_t moe_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t *hi
  *                 normal layout; per expert [E, G, R4] with R4 = roundup(M, 4) in the masked
  *                 layout. UE8M0 bytes are grouped four per int32 word, the words laid out
  *                 the same way ([G/4 rounded up, R4] words per expert / buffer).
+ *                 MOE_SCALES_SWIZZLED_128X4 (NVFP4 only): see moe_scale_layout_t, with the
+ *                 destination rows (row-capacity out_rows, or E*M in the masked layout) as R.
  *   out_rows      normal layout: the row capacity of out_q (>= T*K; T*K + E*(A-1) for
  *                 metadata from moe_route_meta_ex); 0 means T*K. Ignored in masked mode.
  * Everything else as moe_dispatch.
@@ -362,6 +373,25 @@ moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t *hidden_
                                       int32_t invalid_expert_id, float input_global_scale, void *recv_x,
                                       uint8_t *recv_scales, int32_t *recv_topk_ids, float *recv_topk_weights,
                                       int32_t *dev_status, moe_stream_t stream);
+
+/*
+ * moe_dispatch_partitioned_ex -- moe_dispatch_partitioned with a block-scale layout.
+ *
+ * scale_layout MOE_SCALES_SWIZZLED_128X4 writes recv_scales already interleaved, as
+ * FlashinferDispatcher.dispatch (flashinfer.py page) obtains them by applying
+ * nvfp4_block_scale_interleave to the received scales viewed as [P*num_slots, H/16] before the
+ * CUTLASS MoE: R = P*num_slots rows, roundup(R, 128)*H/16 bytes, padding rows zero; slots a
+ * partition does not receive are left untouched as in the row-major layout. NVFP4 only,
+ * H % 64 == 0, recv_scales 4-byte aligned. MOE_SCALES_ROW_MAJOR is moe_dispatch_partitioned.
+ * Everything else as moe_dispatch_partitioned.
+ */
+moe_status_t moe_dispatch_partitioned_ex(moe_quant_t quant, moe_scale_layout_t scale_layout,
+                                         const uint16_t *hidden_states, int64_t num_tokens, int64_t num_slots,
+                                         int hidden, const int32_t *topk_ids, const float *topk_weights, int topk,
+                                         int num_experts, int num_partitions, int32_t invalid_expert_id,
+                                         float input_global_scale, void *recv_x, uint8_t *recv_scales,
+                                         int32_t *recv_topk_ids, float *recv_topk_weights, int32_t *dev_status,
+                                         moe_stream_t stream);
 
 /*
  * moe_combine_partitioned -- the FlashInfer all-to-all combine, one source rank.

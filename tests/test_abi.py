@@ -131,3 +131,35 @@ def test_dispatch_and_combine_argument_validation(lib):
     assert comb(mode=1, M=0) == 1
     assert comb(K=20) == 2
     assert comb(T=0) == 0
+
+
+def test_swizzled_scale_layout_validation(lib):
+    """MOE_SCALES_SWIZZLED_128X4: NVFP4 only, H % 64 == 0, 4-byte aligned scales."""
+    d = _c(lib, "moe_dispatch_ex")
+    d.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p]
+
+    def disp(layout=2, quant=2, T=4, H=256, s=FAKE):
+        return d(0, quant, layout, FAKE, T, H, FAKE, 2, 8, 0, 0, FAKE, FAKE, 1.0, FAKE, s, FAKE, None)
+
+    assert disp(quant=1) == 1                      # FP8 has no swizzled layout
+    assert disp(H=272) == 1                        # 17 scale columns: not whole 4-column tiles
+    assert disp(s=ctypes.c_void_p(0x1002)) == 1    # scales must be 4-byte aligned
+    assert disp(layout=3) == 1
+    assert disp(T=0) == 0
+    p = _c(lib, "moe_dispatch_partitioned_ex")
+    p.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int32,
+                  ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+
+    def part(quant=2, layout=2, H=256, S=0, sf=FAKE):
+        return p(quant, layout, FAKE, 0, S, H, FAKE, FAKE, 2, 8, 2, -1, 1.0, FAKE, sf, FAKE, FAKE, FAKE, None)
+
+    assert part(quant=0) == 1                      # bf16 payload has no scales to swizzle
+    assert part(layout=1) == 1                     # column-major is an FP8 layout
+    assert part(H=80) == 1
+    assert part(sf=ctypes.c_void_p(0x1001)) == 1
+    assert part() == 0                             # no slots: nothing to launch

@@ -253,3 +253,35 @@ def test_ue8m0_bulk_path_normal_layout():
     n = om.num_valid
     assert (gq[n:] == SENTINEL).all() and (gs[n:] == SENTINEL).all()
     assert int(st.item()) == 0
+
+
+# --- NVFP4 block scales in the 128 x 4 swizzled layout (nvfp4_block_scale_interleave) --------
+
+@pytest.mark.parametrize("mode,T,H,E,K,M", [
+    ("normal", 300, 1024, 24, 6, 0),     # 1800 rows -> padded to 1920
+    ("normal", 1500, 2048, 64, 8, 0),    # a batch the row-major NVFP4 path sends to the bulk kernel
+    ("masked", 96, 1024, 16, 4, 30),     # E*M = 480 rows -> padded to 512
+    ("masked", 128, 7168, 256, 8, 128),  # the decode shape: 32768 rows, no padding
+])
+def test_nvfp4_swizzled_scales_match_oracle_interleave(mode, T, H, E, K, M):
+    """The whole scale buffer equals the oracle's row-major scales (untouched rows keep
+    their fill) passed through the interleave: padding rows zero, codes unchanged."""
+    m = moe()
+    w = make_case(T, H, E, K, seed=T + H, mode=mode, quant="nvfp4b16", M=M, invalid_rate=0.05)
+    x, ids, _ = to_dev(w)
+    om = oracle.route_meta(w.topk_ids, E, M=M)
+    seg = torch.from_numpy(om.seg_indptr).cuda()
+    s2d = torch.from_numpy(om.src2dst).cuda()
+    R = T * K if mode == "normal" else E * M
+    q = filled((R, H // 2), torch.uint8)
+    sf = filled((m.swizzled_scale_bytes(R, H),), torch.uint8)
+    st = m.new_status()
+    m.moe_dispatch_ex(mode, "nvfp4b16", "swizzled", x, ids, E, s2d, seg, q, sf, st, max_tokens_per_expert=M,
+                      input_global_scale=w.global_scale)
+    oq, osf = oracle.dispatch(mode, "nvfp4b16", w.x, w.topk_ids, om, E, M=M, global_scale=w.global_scale,
+                              rows=R if mode == "normal" else None, fill=SENTINEL)
+    want_sf = oracle.nvfp4_sf_interleave(osf.reshape(R, H // 16))
+    torch.cuda.synchronize()
+    assert np.array_equal(bytes_of(q).reshape(-1), oq.reshape(-1))
+    assert np.array_equal(sf.cpu().numpy(), want_sf)
+    assert int(st.item()) == 0    # the dispatch drops pairs past capacity silently (route_meta reports them)

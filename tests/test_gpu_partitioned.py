@@ -109,3 +109,32 @@ def test_partitioned_nvfp4_workload_layout_and_sampled_rows():
         for p in set(part[t][part[t] >= 0].tolist()):
             assert np.array_equal(rx[p, t].cpu().numpy(), q) and np.array_equal(rsf[p, t].cpu().numpy(), sf)
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("T,S,H,E,K,P", [
+    (20, 20, 64, 4, 2, 1),            # 20 rows -> padded to 128
+    (50, 61, 1024, 32, 6, 8),         # 488 rows -> padded to 512, padding slots
+    (128, 128, 7168, 256, 8, 8),      # the FlashInfer NVFP4 payload shape, 1024 rows
+])
+def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
+    """moe_dispatch_partitioned_ex with swizzled scales equals the row-major receive scales
+    [P*S, H/16] passed through nvfp4_block_scale_interleave (untouched slots keep their
+    fill, padding rows zero); codes, ids and weights as in the row-major layout."""
+    m = moe()
+    w = make_case(T, H, E, K, seed=T * 5 + P, quant="nvfp4b16", invalid_rate=0.05)
+    x, ids, wt = to_dev(w)
+    rx = filled((P, S, H // 2), torch.uint8)
+    rsf = filled((m.swizzled_scale_bytes(P * S, H),), torch.uint8)
+    rids = filled((P, S, K), torch.int32)
+    rw = filled((P, S, K), torch.float32)
+    st = m.new_status()
+    m.moe_dispatch_partitioned_ex("nvfp4b16", "swizzled", x, ids, wt, E, P, rx, rsf, rids, rw, st,
+                                  input_global_scale=w.global_scale)
+    ox, osf, oids, ow = oracle.dispatch_partitioned("nvfp4b16", w.x, w.topk_ids, w.topk_weights, E, P,
+                                                    global_scale=w.global_scale, num_slots=S, fill=SENTINEL)
+    torch.cuda.synchronize()
+    assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
+    assert np.array_equal(rsf.cpu().numpy(), oracle.nvfp4_sf_interleave(osf.reshape(P * S, H // 16)))
+    assert np.array_equal(rids.cpu().numpy(), oids)
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
+    assert int(st.item()) == 0
