@@ -288,6 +288,127 @@ def config_of(w) -> dict:
                   f"read so no dirty flush lines remain)"}
 
 
+L2_BYTES = 129 << 20  # GB300 L2 (126 MiB reported by the device; rounded up)
+
+
+def run_e2e(args, w, d, dev, x_h, ids_h, wt_h, g, fused, expert_out, dist):
+    """Tokens/s through the public API with every step's inputs copied in from pinned host
+    memory and its combined output copied back, K steps inside the timed region.
+
+    Pipelined as a serving loop would run it: step i+1's host->device copy and step i-1's
+    device->host copy overlap step i's kernels (three streams, two sets of device inputs,
+    dispatcher outputs and pinned output buffers; events order every reuse of a buffer).
+    The L2 is not flushed inside the region: each step's inputs arrive fresh from the host,
+    and the combine reads rotate over enough expert-output buffers that the rows one step
+    reads have left L2 before they are read again. The serial variant (copy in, kernels,
+    copy out, one step at a time) is measured too and reported alongside."""
+    import torch
+    import combine_moe_route_meta_gb300 as moe
+
+    nx, ni, nw = x_h.numel() * 2, ids_h.numel() * 4, wt_h.numel() * 4
+    o_ids = (nx + 15) // 16 * 16
+    o_w = (o_ids + ni + 15) // 16 * 16
+    n_in = (o_w + nw + 15) // 16 * 16
+    host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
+    host_in[:nx].copy_(x_h.view(torch.uint8).reshape(-1))
+    host_in[o_ids:o_ids + ni].copy_(ids_h.view(torch.uint8).reshape(-1))
+    host_in[o_w:o_w + nw].copy_(wt_h.view(torch.uint8).reshape(-1))
+    dev_in = [torch.empty(n_in, dtype=torch.uint8, device=dev) for _ in range(2)]
+    views = [(b[:nx].view(torch.bfloat16).view(w.T, w.H), b[o_ids:o_ids + ni].view(torch.int32).view(w.T, w.K),
+              b[o_w:o_w + nw].view(torch.float32).view(w.T, w.K)) for b in dev_in]
+    ds = [d, moe.MoEDispatcher(w.T, w.H, w.K, w.E, mode=w.mode, quant=w.quant, num_partitions=w.P,
+                               max_tokens_per_expert=w.M, device=dev)]
+    outp = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    # expert-output buffers: the combine of one step reads K rows per token
+    read_per_step = max(1, w.T * w.K * w.H * 2)
+    n_eo = int(min(32, max(1, -(-2 * L2_BYTES // read_per_step))))
+    eos = [expert_out] + [torch.empty_like(expert_out).copy_(expert_out) for _ in range(n_eo - 1)]
+
+    def kernels(slot, i):
+        x2, ids2, wt2 = views[slot]
+        dd = ds[slot]
+        if fused:
+            dd.route_dispatch(x2, ids2, g)
+        else:
+            dd.route(ids2)
+            dd.dispatch(x2, ids2, g)
+        dd.combine(eos[i % n_eo], ids2, wt2)
+
+    s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def pipelined(n):
+        ran = [None, None]   # kernels of the last step in each slot done (dev_in[b] free to refill)
+        out = [None, None]   # device->host copy of the last step in each slot done (ds[b].out free)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for i in range(n):
+            b = i & 1
+            if ran[b] is not None:
+                s_in.wait_event(ran[b])
+            with torch.cuda.stream(s_in):
+                dev_in[b].copy_(host_in, non_blocking=True)
+            e_in = torch.cuda.Event()
+            e_in.record(s_in)
+            s_run.wait_event(e_in)
+            if out[b] is not None:
+                s_run.wait_event(out[b])
+            with torch.cuda.stream(s_run):
+                kernels(b, i)
+            ran[b] = torch.cuda.Event()
+            ran[b].record(s_run)
+            s_out.wait_event(ran[b])
+            with torch.cuda.stream(s_out):
+                outp[b].copy_(ds[b].out, non_blocking=True)
+            out[b] = torch.cuda.Event()
+            out[b].record(s_out)
+        t1.record(s_out)
+        return t0, t1
+
+    def serial(n):
+        evs = []
+        with torch.cuda.stream(s_run):
+            for i in range(n):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s_run)
+                dev_in[0].copy_(host_in, non_blocking=True)
+                kernels(0, i)
+                outp[0].copy_(ds[0].out, non_blocking=True)
+                e1.record(s_run)
+                evs.append((e0, e1))
+        return evs
+
+    torch.cuda.synchronize()
+    pipelined(max(args.warmup, 2))
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = pipelined(args.steps)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    for dd in ds:
+        dd.check()
+    last = (args.steps - 1) & 1
+    assert torch.equal(outp[last], ds[last].out.cpu()), "e2e output differs from the device result"
+    ms_pipe = max_over_ranks(t0.elapsed_time(t1) / args.steps, dist, dev)
+
+    serial(max(args.warmup, 2))
+    torch.cuda.synchronize()
+    evs = serial(args.steps)
+    torch.cuda.synchronize()
+    ms_serial = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in evs), dist, dev)
+    world = dist.get_world_size() if dist else 1
+    return {"value": job_throughput(w.T, world, ms_pipe), "unit": "tokens/s", "ms_per_step": ms_pipe,
+            "h2d_bytes_per_step": n_in, "d2h_bytes_per_step": w.T * w.H * 2,
+            "copies": "one pinned H2D of the step's inputs, one D2H of the combined output, every step",
+            "schedule": "pipelined: copies of neighbouring steps overlap this step's kernels (3 streams, 2 buffer sets)",
+            "l2": f"not flushed; inputs arrive by H2D each step; combine reads rotate over {n_eo} expert-output buffers",
+            "serial": {"value": job_throughput(w.T, world, ms_serial), "ms_per_step": ms_serial,
+                       "schedule": "copy in, kernels, copy out, one step after another"}}
+
+
 def run_gpu(args, w, rank, world, dist):
     import torch
     import combine_moe_route_meta_gb300 as moe
@@ -410,50 +531,7 @@ def run_gpu(args, w, rank, world, dist):
     # ---- end to end through the public API: pinned host in, host out ----
     e2e = None
     if not args.no_e2e:
-        # the step's three inputs live in one pinned host buffer and move in one copy;
-        # the combined output comes back in one copy
-        nx, ni, nw = x_h.numel() * 2, ids_h.numel() * 4, wt_h.numel() * 4
-        o_ids = (nx + 15) // 16 * 16
-        o_w = (o_ids + ni + 15) // 16 * 16
-        n_in = (o_w + nw + 15) // 16 * 16
-        host_in = torch.empty(n_in, dtype=torch.uint8).pin_memory()
-        host_in[:nx].copy_(x_h.view(torch.uint8).reshape(-1))
-        host_in[o_ids:o_ids + ni].copy_(ids_h.view(torch.uint8).reshape(-1))
-        host_in[o_w:o_w + nw].copy_(wt_h.view(torch.uint8).reshape(-1))
-        dev_in = torch.empty(n_in, dtype=torch.uint8, device=dev)
-        x2 = dev_in[:nx].view(torch.bfloat16).view(w.T, w.H)
-        ids2 = dev_in[o_ids:o_ids + ni].view(torch.int32).view(w.T, w.K)
-        wt2 = dev_in[o_w:o_w + nw].view(torch.float32).view(w.T, w.K)
-        outp = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-
-        def e2e_step():
-            dev_in.copy_(host_in, non_blocking=True)
-            if fused:
-                d.route_dispatch(x2, ids2, g)
-            else:
-                d.route(ids2)
-                d.dispatch(x2, ids2, g)
-            y = d.combine(expert_out, ids2, wt2)
-            outp.copy_(y, non_blocking=True)
-
-        for i in range(max(args.warmup, 1)):
-            flush_l2(i)
-            e2e_step()
-        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        torch.cuda.synchronize()
-        for i in range(args.steps):
-            flush_l2(i)
-            ev2[i][0].record(stream)
-            e2e_step()
-            ev2[i][1].record(stream)
-        torch.cuda.synchronize()
-        d.check()
-        assert torch.equal(outp, d.out.cpu()), "e2e output differs from the device result"
-        ms2 = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev2), dist, dev)
-        e2e = {"value": job_throughput(w.T, world, ms2), "unit": "tokens/s", "ms_per_step": ms2,
-               "h2d_bytes_per_step": n_in, "d2h_bytes_per_step": w.T * w.H * 2,
-               "copies": "one pinned H2D of the step's inputs, one D2H of the combined output"}
+        e2e = run_e2e(args, w, d, dev, x_h, ids_h, wt_h, g, fused, expert_out, dist)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
