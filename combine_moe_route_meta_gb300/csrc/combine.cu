@@ -80,7 +80,6 @@ __device__ __forceinline__ int64_t slot_row(const CombineArgs& a, const int* s_s
 template <bool MASKED>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a) {
     extern __shared__ int s_seg[];  // [E] in masked mode
-    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;

@@ -88,7 +88,6 @@ __device__ __forceinline__ int64_t dest_row(const DispatchArgs& a, const int* s_
 template <int QUANT, bool MASKED>
 __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs a) {
     extern __shared__ int s_seg[];  // [E] in masked mode
-    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -150,7 +149,6 @@ __device__ __forceinline__ void stage_seg(const DispatchArgs& a, int* s_seg) {
 template <bool MASKED>
 __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(DispatchArgs a, BulkGeom geo) {
     extern __shared__ __align__(128) unsigned char smem[];
-    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31, NS = geo.stages;
     const uint32_t bar0 = smem_addr(smem), in0 = smem_addr(smem + geo.in_off);
@@ -207,7 +205,6 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
 template <int QUANT, bool MASKED>
 __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(DispatchArgs a, BulkGeom geo) {
     extern __shared__ __align__(128) unsigned char smem[];
-    pdl_launch_dependents();
     pdl_wait();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
     const int NS = geo.stages, H = a.H;
@@ -409,7 +406,6 @@ cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t 
 // Zeros of the padding rows [R, roundup(R, 128)) of a 128 x 4 swizzled scale matrix with C
 // columns (C % 4 == 0): one thread per 4-byte word (row, tile column).
 __global__ void sf_swizzle_pad_kernel(uint8_t* sf, int64_t R, int C, int64_t n_words) {
-    pdl_launch_dependents();
     pdl_wait();
     const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (j >= n_words) return;

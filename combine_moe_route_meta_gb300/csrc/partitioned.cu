@@ -38,7 +38,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_layout_kernel(const int32_t
                                                                     int K, int E, int P, int32_t* ntr,
                                                                     uint8_t* itr, int32_t* nte, int32_t* status) {
     extern __shared__ int s_cnt[];  // [P] tokens per partition, then [E] pairs per expert
-    pdl_launch_dependents();
     pdl_wait();
     int* s_rank = s_cnt;
     int* s_exp = s_cnt + P;
@@ -110,7 +109,6 @@ __device__ __forceinline__ bool token_in_partition(const PartArgs& a, int64_t t,
 
 template <int QUANT>
 __global__ void __launch_bounds__(kThreads) dispatch_partitioned_kernel(PartArgs a) {
-    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -155,7 +153,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_partitioned_kernel(PartArgs
 }
 
 __global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs a) {
-    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;

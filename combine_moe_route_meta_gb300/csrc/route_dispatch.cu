@@ -126,7 +126,6 @@ __device__ void fused_global_metadata(const FusedArgs& a, int* smem) {
 template <int QUANT, bool MASKED, int KMAX>
 __global__ void route_dispatch_small_kernel(FusedArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    pdl_launch_dependents();  // a programmatic dependent (the combine) may start launching
     pdl_wait();               // the previous kernel's writes (ids, hidden_states) are visible
     if (blockIdx.x == unsigned(a.T)) {
         fused_global_metadata(a, reinterpret_cast<int*>(smem_raw));

@@ -216,7 +216,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_single_kernel(Rou
     int* warp_sums = seg + E + 1;
     for (int j = threadIdx.x; j < kWarps * S; j += blockDim.x) cnt[j] = 0;
     __syncthreads();
-    pdl_launch_dependents();
     pdl_wait();
 
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,7 +256,6 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_count_kernel(Rout
     int* hist = cnt + kWarps * S;
     for (int j = threadIdx.x; j < kWarps * S; j += blockDim.x) cnt[j] = 0;
     __syncthreads();
-    pdl_launch_dependents();  // the place kernel may start launching (it waits for us)
     pdl_wait();
 
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -328,7 +326,6 @@ __device__ void table_column_sums(const int32_t* table, int B, int b, int E, int
 // shared memory: part_pre[G][E] | part_tot[G][E] | tot[E] | pre[E] | seg[E+1] | warp_sums[32]
 __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteArgs a) {
     extern __shared__ int smem[];
-    pdl_launch_dependents();
     pdl_wait();
     const int E = a.E, B = gridDim.x, b = blockIdx.x, tid = threadIdx.x;
     const int G = table_cols_g(E);
