@@ -168,10 +168,11 @@ class ClockSampler:
 _ORACLE_OUT = {}
 
 
-def _oracle_out(w, T_s):
-    """Dispatch output arrays for a T_s-token sample, allocated once (outside any timing)."""
+def _oracle_out(w, T_s, slot: int = 0):
+    """Dispatch output arrays for a T_s-token sample, allocated once (outside any timing);
+    `slot` gives each concurrent caller its own arrays."""
     import oracle
-    key = (w.name, w.seed, T_s)
+    key = (w.name, w.seed, T_s, slot)
     if key not in _ORACLE_OUT:
         rows = None if w.mode == "masked" else T_s * w.K
         qs, qd, ss, sd = oracle.out_shapes(w.mode, w.quant, T_s, w.H, w.K, w.E, w.M, rows)
@@ -179,7 +180,7 @@ def _oracle_out(w, T_s):
     return _ORACLE_OUT[key]
 
 
-def oracle_step(w, T_s: int, expert_rows):
+def oracle_step(w, T_s: int, expert_rows, slot: int = 0):
     """One oracle pass (route meta + dispatch + combine) over the first T_s tokens."""
     import oracle
     ids = np.ascontiguousarray(w.topk_ids[:T_s])
@@ -188,7 +189,7 @@ def oracle_step(w, T_s: int, expert_rows):
     meta = oracle.route_meta(ids, w.E, P=w.P, M=w.M)
     rows = None if w.mode == "masked" else T_s * w.K
     oracle.dispatch(w.mode, w.quant, x, ids, meta, w.E, M=w.M, global_scale=w.global_scale or 0.0, rows=rows,
-                    out=_oracle_out(w, T_s))
+                    out=_oracle_out(w, T_s, slot))
     if w.mode == "normal":
         eo = expert_rows[: max(meta.num_valid, 1)]
         oracle.combine("normal", eo, ids, wt, meta, w.E)
@@ -201,18 +202,28 @@ def oracle_step(w, T_s: int, expert_rows):
         oracle.combine("masked", eo, ids, wt, meta_s, w.E, M=M_s)
 
 
+def _expert_rows_needed(w, T_s: int) -> int:
+    """Expert-output rows the oracle's combine reads for a T_s-token sample: T_s*K in the
+    contiguous layout, E x (largest per-expert count of the sample) in the masked one."""
+    if w.mode == "normal":
+        return max(T_s * w.K, 1)
+    import oracle
+    meta = oracle.route_meta(np.ascontiguousarray(w.topk_ids[:T_s]), w.E, P=w.P, M=w.M)
+    return w.E * max(int(meta.masked_m.max()) if meta.num_valid else 1, 1)
+
+
 def time_oracle(w, budget_s: float, max_tokens: int):
     """Pick a token sample that takes ~budget_s per step and time one step of it."""
     from workloads import random_bf16
     rng = np.random.default_rng(99)
     T_probe = min(w.T, 16)
-    er = random_bf16(rng, (max(w.E * max(T_probe, 1), T_probe * w.K, 1), w.H))
+    er = random_bf16(rng, (_expert_rows_needed(w, T_probe), w.H))
     oracle_step(w, T_probe, er)  # allocates the sample's output arrays
     t0 = time.perf_counter()
     oracle_step(w, T_probe, er)
     per_tok = (time.perf_counter() - t0) / T_probe
     T_s = int(max(1, min(w.T, max_tokens, budget_s / max(per_tok, 1e-9))))
-    er = random_bf16(rng, (max(w.E * T_s, T_s * w.K, 1), w.H))
+    er = random_bf16(rng, (_expert_rows_needed(w, T_s), w.H))
     _oracle_out(w, T_s)
     return T_s, er
 
@@ -231,6 +242,34 @@ def cpu_baseline(w, budget_s: float = 12.0) -> dict:
     return {"value": T_s / med, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"first {T_s} of {w.T} tokens of the {w.name} workload, route+dispatch+combine, "
                       f"median of {len(times)} passes, single-threaded C oracle"}
+
+
+def cpu_baseline_all_cores(w, budget_s: float = 10.0) -> dict:
+    """The same oracle, unchanged, run concurrently on every host core: one thread per core,
+    each repeating the single-core sample on its own output arrays (the oracle's C calls
+    release the interpreter lock). Tokens of all threads / wall time."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = os.cpu_count() or 1
+    T_s, er = time_oracle(w, budget_s / 4, w.T)
+    for j in range(n):
+        _oracle_out(w, T_s, j)
+    oracle_step(w, T_s, er)
+    t_one = time.perf_counter()
+    oracle_step(w, T_s, er)
+    t_one = time.perf_counter() - t_one
+    passes = int(max(1, min(50, budget_s / max(t_one, 1e-9) / 2)))
+
+    def work(j):
+        for _ in range(passes):
+            oracle_step(w, T_s, er, slot=j)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(work, range(n)))
+    wall = time.perf_counter() - t0
+    return {"value": n * passes * T_s / wall, "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "sample": f"{n} threads, each {passes} passes over the first {T_s} of {w.T} tokens of the "
+                      f"{w.name} workload (route+dispatch+combine), single-threaded C oracle per thread"}
 
 
 def run_reference(args, w, rank, world):
@@ -622,11 +661,49 @@ def run_gpu(args, w, rank, world, dist):
     ev = timed_pass(timed_step)
     # pass 2: the same K steps, eager, with an event after every kernel: per-kernel durations
     ev_k = timed_pass(kernel_timed_step)
+    # pass 3: one step captured as a CUDA graph, replayed K times after an L2 flush each (cold)
+    # and K times back to back (warm: the step's working set may stay in L2)
+    g_step = graph
+    if g_step is None:
+        s3 = torch.cuda.Stream()
+        s3.wait_stream(stream)
+        with torch.cuda.stream(s3):
+            step()
+        stream.wait_stream(s3)
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            step()
+
+    def graph_cold(i, e):
+        flush_l2(i)
+        e[0].record(stream)
+        g_step.replay()
+        e[3].record(stream)
+
+    ev_g = timed_pass(graph_cold)
+    for _ in range(args.warmup):
+        g_step.replay()
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    w0.record(stream)
+    for _ in range(args.steps):
+        g_step.replay()
+    w1.record(stream)
+    torch.cuda.synchronize()
     clocks = sampler.stop()
     d.check()
+    ms_gc = max_over_ranks(statistics.mean(e[0].elapsed_time(e[3]) for e in ev_g), dist, dev)
+    ms_gw = max_over_ranks(w0.elapsed_time(w1) / args.steps, dist, dev)
+    graph_replay = {"cold_l2": {"ms_per_step": ms_gc, "value": job_throughput(w.T, world, ms_gc)},
+                    "warm_l2": {"ms_per_step": ms_gw, "value": job_throughput(w.T, world, ms_gw)},
+                    "timing": "one step captured as a CUDA graph; cold: L2 flushed before each replay; "
+                              "warm: K replays back to back"}
 
     step_ms = [e[0].elapsed_time(e[3]) for e in ev]
     ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
+    ms_median = max_over_ranks(statistics.median(step_ms), dist, dev)
     value = job_throughput(w.T, world, ms)
     ms_k = max_over_ranks(statistics.mean(e[0].elapsed_time(e[3]) for e in ev_k), dist, dev)
 
@@ -659,11 +736,14 @@ def run_gpu(args, w, rank, world, dist):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy PCG64 inputs, random expert outputs)",
+        "ms_per_step_median": ms_median,
         "ms_per_step_with_kernel_events": ms_k,
+        "graph_replay": graph_replay,
         "config": dict(config_of(w), timing=(("CUDA graph of one step, replayed per step" if graph is not None
                                               else "eager launches") + ", CUDA events around each step; then "
                                              "K more eager steps with an event after every kernel give the "
-                                             "per-kernel durations"),
+                                             "per-kernel durations; graph_replay: the step as a CUDA graph, "
+                                             "cold and warm L2"),
                        fused_route_dispatch=fused, n_valid_pairs=n_valid, rows_moved=n_rows),
         "achieved_gbs_step": step_bytes / (ms * 1e-3) / 1e9 / max(world, 1) * world,
         "step_algorithmic_bytes": step_bytes,
@@ -722,11 +802,13 @@ def main():
         dist.barrier()
 
     w = make_workload(args.workload, seed=rank_seed(rank))
-    cpu = None
+    cpu = cpu_all = None
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
+        cpu_all = cpu_baseline_all_cores(w)
     line = run_gpu(args, w, rank, world, dist)
     line["cpu_baseline"] = cpu
+    line["cpu_baseline_all_cores"] = cpu_all
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
