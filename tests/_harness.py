@@ -42,9 +42,31 @@ def bytes_of(t: torch.Tensor) -> np.ndarray:
     return a.reshape(rows, width)
 
 
+GUARD_BYTES = 4096
+_GUARDED = []  # (whole allocation, inner bytes, fill) of every buffer made by filled()
+
+
 def filled(shape, dtype, fill=SENTINEL) -> torch.Tensor:
+    """A device buffer of `shape` filled with the byte `fill`, placed between two guard
+    margins of GUARD_BYTES holding the same byte; check_guards() verifies that no kernel
+    wrote outside the buffer (the canary check used instead of a memory checker)."""
     n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
-    return torch.full((n,), fill, dtype=torch.uint8, device="cuda").view(dtype).view(shape)
+    whole = torch.full((n + 2 * GUARD_BYTES,), fill, dtype=torch.uint8, device="cuda")
+    _GUARDED.append((whole, n, fill))
+    return whole[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+
+
+def check_guards():
+    """Every guard margin of the buffers made by filled() since the last check still holds
+    its fill byte."""
+    torch.cuda.synchronize()
+    try:
+        for whole, n, fill in _GUARDED:
+            margins = torch.cat([whole[:GUARD_BYTES], whole[GUARD_BYTES + n:]])
+            bad = int((margins != fill).sum().item())
+            assert bad == 0, f"{bad} guard bytes around a {n}-byte output buffer were overwritten"
+    finally:
+        _GUARDED.clear()
 
 
 def check_meta(w: Workload, om: oracle.Meta, gm, status: torch.Tensor):

@@ -31,3 +31,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _guard_canaries(request):
+    """After every GPU test: no output buffer made by the harness was written out of bounds."""
+    yield
+    if HAS_GPU and "gpu" in request.keywords:
+        from _harness import check_guards
+        check_guards()

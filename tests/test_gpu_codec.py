@@ -2,8 +2,9 @@
 moe_convert_probe, against the oracle's format definitions on every decision point --
 each representable value, every midpoint between neighbours and the float32 values up
 to 3 ulps either side of it, saturation, signed zeros, float32 subnormals -- plus a
-million log-uniform random values. Also fixes the packing order: the even element goes
-to the low byte (e4m3 pair) / low nibble (e2m1 pair)."""
+million log-uniform random values; and exhaustively over every float32 whose conversion is
+not a trivial saturation or flush to zero. Also fixes the packing order: the even element
+goes to the low byte (e4m3 pair) / low nibble (e2m1 pair)."""
 import numpy as np
 import pytest
 import torch
@@ -66,3 +67,39 @@ def test_convert_probe_matches_oracle_formats():
     od = np.array([oracle.e4m3_to_float(c) for c in range(256)], np.float64)[o4].astype(np.float32)
     ok = ~np.isnan(od)
     assert np.array_equal(gd[ok].view(np.uint32), od[ok].view(np.uint32))
+
+
+def test_convert_probe_exhaustive_over_the_rounding_range():
+    """Every float32 of both signs with magnitude in [2^-11, 2^11) -- the range in which an
+    e4m3 or e2m1 conversion neither saturates trivially nor flushes to zero (e4m3: smallest
+    subnormal 2^-9, largest finite 448; e2m1: 0.5 .. 6) -- in chunks of 2^25 values:
+    369 million conversions of each kind compared with the oracle's definitions."""
+    m = moe()
+    lo, hi = (127 - 11) << 23, (127 + 11) << 23
+    chunk = 1 << 25
+    table = np.array([oracle.e4m3_to_float(c) for c in range(256)], np.float64).astype(np.float32)
+    x = torch.empty(chunk, dtype=torch.float32, device="cuda")
+    e4 = torch.empty(chunk, dtype=torch.uint8, device="cuda")
+    e2 = torch.empty(chunk // 2, dtype=torch.uint8, device="cuda")
+    dv = torch.empty(chunk, dtype=torch.float32, device="cuda")
+    checked = 0
+    for sign in (0, 1 << 31):
+        for start in range(lo, hi, chunk):
+            n = min(chunk, hi - start)
+            bits = np.arange(start, start + n, dtype=np.uint64).astype(np.uint32) | np.uint32(sign)
+            v = bits.view(np.float32)
+            x[:n].copy_(torch.from_numpy(v))
+            m.moe_convert_probe(x[:n], e4[:n], e2[: n // 2], dv[:n])
+            g4, g2, gd = e4[:n].cpu().numpy(), e2[: n // 2].cpu().numpy(), dv[:n].cpu().numpy()
+            o4 = oracle.e4m3_from_float_array(v)
+            bad = np.nonzero(g4 != o4)[0]
+            assert bad.size == 0, [(float(v[i]), hex(g4[i]), hex(o4[i])) for i in bad[:8]]
+            o2 = oracle.e2m1_from_float_array(v)
+            packed = (o2[0::2] | (o2[1::2] << 4)).astype(np.uint8)
+            bad = np.nonzero(g2 != packed)[0]
+            assert bad.size == 0, [(float(v[2 * i]), hex(g2[i]), hex(packed[i])) for i in bad[:8]]
+            od = table[o4]
+            ok = ~np.isnan(od)
+            assert np.array_equal(gd[ok].view(np.uint32), od[ok].view(np.uint32))
+            checked += n
+    assert checked == 2 * (hi - lo)
