@@ -7,10 +7,11 @@
 // row = src2dst (normal) or e*M + rank (masked); fp32 fused multiply-add accumulation.
 //
 // Design: HBM-bound K-way gather. One warp per (token, 512-column slice); each lane owns
-// 16 columns. Lanes 0..K-1 fetch the slot metadata (row, weight) and broadcast it by
-// shuffle (the masked layout reads seg_indptr from a shared-memory copy). Each lane then
-// issues the loads of up to 8 source rows (2 x 16 B per row, ld.global.nc with
-// L1::no_allocate) before consuming any, so a warp keeps 8 KB in flight, and the next
+// 16 columns, as two runs of 8 placed 256 columns apart so that each warp-wide 16-byte load
+// covers 512 contiguous bytes. Lanes 0..K-1 fetch the slot metadata (row, weight) and
+// broadcast it by shuffle (the masked layout reads seg_indptr from a shared-memory copy).
+// Each lane then issues the loads of up to 8 source rows (2 x 16 B per row, ld.global.nc
+// with L1::no_allocate) before consuming any, so a warp keeps 8 KB in flight, and the next
 // unit's slot metadata is fetched alongside. Accumulation order is fixed (k ascending)
 // and the result is rounded once to bf16 (cvt.rn.bf16x2). A token with no valid slot
 // gets zeros. Small grids use smaller blocks so that every SM gets a similar share.
@@ -24,7 +25,8 @@ namespace {
 
 constexpr int kCombineThreads = 256;
 constexpr int kSlice = 512;
-constexpr int kLaneElems = 16;
+constexpr int kLaneElems = 16;  // per lane and slice: two runs of kHalfElems
+constexpr int kHalfElems = 8;
 constexpr int kBatch = 8;  // source rows in flight per lane
 
 struct CombineArgs {
@@ -96,8 +98,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
 
     for (; u < a.n_units; u += nwarps) {
         const int64_t t = u / a.units_per_row;
-        const int col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
-        const bool active = col < H;
+        // lane l owns columns [8l, 8l+8) and [256+8l, 256+8l+8) of the slice, so each of the
+        // warp's two 16-byte loads per row reads 512 contiguous bytes (whole 32-byte sectors)
+        const int col0 = int(u - t * a.units_per_row) * kSlice + lane * kHalfElems;
+        const int col1 = col0 + kSlice / 2;
+        const bool act0 = col0 < H, act1 = col1 < H;  // act1 implies act0
         const int64_t my_row = slot_row<MASKED>(a, s_seg, meta);
         const float my_w = meta.w;
 
@@ -113,18 +118,17 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
                 const int k = k0 + j;
                 rows[j] = __shfl_sync(kFullMask, my_row, k & 31);
                 wk[j] = __shfl_sync(kFullMask, my_w, k & 31);
-                if (k >= a.K || !active) rows[j] = -1;
+                if (k >= a.K || !act0) rows[j] = -1;
             }
             uint4 v[kBatch][2];
 #pragma unroll
             for (int j = 0; j < kBatch; j++) {
+                v[j][0] = make_uint4(0, 0, 0, 0);
+                v[j][1] = v[j][0];
                 if (rows[j] >= 0) {
-                    const uint16_t* p = a.eo + rows[j] * H + col;
-                    v[j][0] = ld_stream_v4(p);
-                    v[j][1] = ld_stream_v4(p + 8);
-                } else {
-                    v[j][0] = make_uint4(0, 0, 0, 0);
-                    v[j][1] = v[j][0];
+                    const uint16_t* p = a.eo + rows[j] * H;
+                    v[j][0] = ld_stream_v4(p + col0);
+                    if (act1) v[j][1] = ld_stream_v4(p + col1);
                 }
             }
             // the next unit's slot metadata rides along with this unit's row loads
@@ -143,13 +147,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
                 }
             }
         }
-        if (active) {
-            uint16_t* dst = a.out + t * H + col;
-            st_v4(dst, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
-            st_v4(dst + 8, make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                      pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
-        }
+        uint16_t* dst = a.out + t * H;
+        if (act0)
+            st_v4(dst + col0, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+        if (act1)
+            st_v4(dst + col1, make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                         pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
     }
 }
 

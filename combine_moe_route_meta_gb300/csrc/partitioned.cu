@@ -161,8 +161,11 @@ __global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs 
     constexpr int kBatch = 8;
     for (int64_t u = warp; u < a.n_units; u += nwarps) {
         const int64_t t = u / a.units_per_row;
-        const int col = int(u - t * a.units_per_row) * kSlice + lane * kLaneElems;
-        const bool active = col < H;
+        // lane l owns columns [8l, 8l+8) and [256+8l, 256+8l+8) of the slice: each warp-wide
+        // 16-byte load reads 512 contiguous bytes
+        const int col0 = int(u - t * a.units_per_row) * kSlice + lane * 8;
+        const int col1 = col0 + kSlice / 2;
+        const bool act0 = col0 < H, act1 = col1 < H;  // act1 implies act0
         int my_id;
         const bool routed = token_in_partition(a, t, lane, my_id);
         const int64_t my_row = routed ? int64_t(lane) * a.S + t : -1;
@@ -174,18 +177,17 @@ __global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs 
 #pragma unroll
             for (int j = 0; j < kBatch; j++) {
                 rows[j] = __shfl_sync(kFullMask, my_row, (p0 + j) & 31);
-                if (p0 + j >= a.P || !active) rows[j] = -1;
+                if (p0 + j >= a.P || !act0) rows[j] = -1;
             }
             uint4 v[kBatch][2];
 #pragma unroll
             for (int j = 0; j < kBatch; j++) {
+                v[j][0] = make_uint4(0, 0, 0, 0);
+                v[j][1] = v[j][0];
                 if (rows[j] >= 0) {
-                    const uint16_t* src = a.partial + rows[j] * H + col;
-                    v[j][0] = ld_stream_v4(src);
-                    v[j][1] = ld_stream_v4(src + 8);
-                } else {
-                    v[j][0] = make_uint4(0, 0, 0, 0);
-                    v[j][1] = v[j][0];
+                    const uint16_t* src = a.partial + rows[j] * H;
+                    v[j][0] = ld_stream_v4(src + col0);
+                    if (act1) v[j][1] = ld_stream_v4(src + col1);
                 }
             }
 #pragma unroll
@@ -199,13 +201,13 @@ __global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs 
                 }
             }
         }
-        if (active) {
-            uint16_t* dst = a.out + t * H + col;
-            st_v4(dst, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
-            st_v4(dst + 8, make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                      pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
-        }
+        uint16_t* dst = a.out + t * H;
+        if (act0)
+            st_v4(dst + col0, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                         pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+        if (act1)
+            st_v4(dst + col1, make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                         pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
     }
 }
 
