@@ -65,6 +65,7 @@ _SIGNATURES = {
     "moe_dispatch": (_int, [_int, _int, _P, _i64, _int, _P, _int, _int, _int, _P, _P, _f32, _P, _P, _P, _P]),
     "moe_combine": (_int, [_int, _P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P]),
     "moe_convert_probe": (_int, [_P, _i64, _P, _P, _P, _P]),
+    "moe_fp8_division_check": (_int, [_P, _P]),
     "moe_route_meta_noalloc": (_int, [_P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_route_dispatch": (_int, [_int, _int, _P, _i64, _int, _P, _int, _int, _int, _int, _f32, _P, _P, _P, _P,
                                   _P, _P, _P, _sz, _P, _P, _P, _P]),
@@ -232,6 +233,14 @@ def moe_convert_probe(x: torch.Tensor, e4m3: Optional[torch.Tensor] = None, e2m1
     """Diagnostics: the quantisers' e4m3 / e2m1 conversions applied to fp32 values ``x``."""
     st = load_library().moe_convert_probe(_ptr(x), x.numel(), _ptr(e4m3), _ptr(e2m1), _ptr(e4m3_value), _stream(stream))
     _check(st, "moe_convert_probe")
+
+
+def moe_fp8_division_check(result: torch.Tensor, stream=None) -> None:
+    """Diagnostics: result ([4] int64) <- (pairs with different e4m3 codes, the first of them,
+    quotient differences with |x/s| >= 2^-12, all quotient differences) of the FP8 quantiser's
+    division against the IEEE division over its whole input domain."""
+    st = load_library().moe_fp8_division_check(_ptr(result), _stream(stream))
+    _check(st, "moe_fp8_division_check")
 
 
 def moe_route_meta_ex(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torch.Tensor, src2dst: torch.Tensor,

@@ -396,6 +396,45 @@ __global__ void convert_probe_kernel(const float* __restrict__ in, int64_t n_pai
 
 }  // namespace
 
+// Exhaustive check of div_by_scale against the IEEE division over the FP8 quantiser's
+// domain: amax = every non-negative finite bf16 (bit patterns 0 .. 0x7F7F, increasing in
+// value; 0 is clamped to 1e-10 as the quantiser does), s = max(amax, 1e-10) / 448, and every
+// bf16 x of either sign with |x| <= amax.
+//   result[0]  pairs whose e4m3 codes differ (the quantiser's output)
+//   result[1]  the first such pair: x bits << 32 | s bits
+//   result[2]  pairs whose quotients differ while |x / s| >= 2^-12 (codes there are not zero)
+//   result[3]  pairs whose quotients differ at all (only where the remainder x - q*s falls
+//              below the normal range, |x| < 2^-103, so |x / s| < 2^-61 and the code is a zero)
+__global__ void __launch_bounds__(256) fp8_division_check_kernel(unsigned long long* result) {
+    for (int a = blockIdx.x; a <= 0x7F7F; a += gridDim.x) {
+        const float amax = __uint_as_float(uint32_t(a) << 16);
+        const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+        const float y = __frcp_rn(sc);
+        for (int xb = threadIdx.x; xb <= a; xb += blockDim.x) {
+#pragma unroll
+            for (int sign = 0; sign < 2; sign++) {
+                const float x = __uint_as_float((uint32_t(xb) << 16) | (sign ? 0x80000000u : 0u));
+                const float want = __fdiv_rn(x, sc), got = div_by_scale(x, sc, y);
+                if (__float_as_uint(want) == __float_as_uint(got)) continue;
+                atomicAdd(result + 3, 1ull);
+                if (fabsf(want) >= 0x1p-12f) atomicAdd(result + 2, 1ull);
+                const uint32_t codes = e4m3x2(want, got);  // low byte: IEEE quotient's code
+                if ((codes & 0xffu) != (codes >> 8)) {
+                    if (atomicAdd(result, 1ull) == 0ull)
+                        result[1] = (static_cast<unsigned long long>(__float_as_uint(x)) << 32) | __float_as_uint(sc);
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_fp8_division_check(const LaunchCtx& ctx, unsigned long long* result) {
+    cudaError_t err = cudaMemsetAsync(result, 0, 4 * sizeof(unsigned long long), ctx.stream);
+    if (err != cudaSuccess) return err;
+    fp8_division_check_kernel<<<ctx.num_sms * 8, 256, 0, ctx.stream>>>(result);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t n, uint8_t* e4m3,
                                  uint8_t* e2m1, float* e4m3_value) {
     const int64_t pairs = n / 2;

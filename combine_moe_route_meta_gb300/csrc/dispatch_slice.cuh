@@ -9,8 +9,9 @@
 //   fp8:   s = max(amax, 1e-10) / 448,           q = e4m3(x / s)
 //   nvfp4: sf = e4m3((amax / 6) * g),             q = e2m1(x * (g / value(sf))), 0 if sf == 0
 // Every division and multiplication is an explicit round-to-nearest binary32 operation
-// (__fdiv_rn / __fmul_rn) and the conversions are cvt.rn.satfinite, so the codes are a
-// deterministic function of the input bits.
+// (__fdiv_rn / __fmul_rn; x / s as a correctly rounded quotient from the reciprocal, see
+// div_by_scale) and the conversions are cvt.rn.satfinite, so the codes are a deterministic
+// function of the input bits.
 #pragma once
 
 #include "moe_device.cuh"
@@ -48,6 +49,21 @@ __device__ __forceinline__ int64_t scale_index(const ScaleLayout& L, int64_t row
     if (!packed4) return (e * G + g) * L.rows_al + r;
     const int G4 = (G + 3) / 4;
     return ((e * G4 + g / 4) * L.rows_al + r) * 4 + (g & 3);
+}
+
+// x / s rounded to nearest even in binary32, given y = 1/s rounded to nearest even, by one
+// correction step after P. W. Markstein ("Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q = x*y lies within an ulp of
+// x/s, the remainder x - q*s is exact in one fused multiply-add, and q + remainder*y rounded
+// once is the correctly rounded quotient -- unless the remainder leaves the normal range
+// (|x| < 2^-103 here), where |x/s| < 2^-61 and the e4m3 code is a signed zero either way.
+// moe_fp8_division_check compares the codes with those of the IEEE division over every
+// (x, s) pair the FP8 quantiser can meet.
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+    const float q = __fmul_rn(x, y);
+    const float r = __fmaf_rn(-q, s, x);
+    // a zero remainder means q is exact; adding it would also turn -0 into +0
+    return r == 0.0f ? q : __fmaf_rn(r, y, q);
 }
 
 // One lane's payload: 16 bf16 elements (two 16-byte vectors) of a token row.
@@ -89,10 +105,11 @@ __device__ __forceinline__ LaneCodes quantise16(const LaneSlice& s, float g) {
         const float sc = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
         uint32_t w[4];
         if constexpr (QUANT == MOE_QUANT_FP8_G128) {
+            const float y = __frcp_rn(sc);
 #pragma unroll
             for (int p = 0; p < 4; p++) {
-                const uint32_t lo = e4m3x2(__fdiv_rn(f[4 * p], sc), __fdiv_rn(f[4 * p + 1], sc));
-                const uint32_t hi = e4m3x2(__fdiv_rn(f[4 * p + 2], sc), __fdiv_rn(f[4 * p + 3], sc));
+                const uint32_t lo = e4m3x2(div_by_scale(f[4 * p], sc, y), div_by_scale(f[4 * p + 1], sc, y));
+                const uint32_t hi = e4m3x2(div_by_scale(f[4 * p + 2], sc, y), div_by_scale(f[4 * p + 3], sc, y));
                 w[p] = lo | (hi << 16);
             }
             out.scale = __float_as_uint(sc);

@@ -397,6 +397,14 @@ moe_status_t moe_combine_partitioned(const uint16_t* partial, int64_t num_tokens
                                                      num_experts, num_partitions, out, dev_status));
 }
 
+moe_status_t moe_fp8_division_check(unsigned long long* result, moe_stream_t stream) {
+    if (!result || !aligned(result, 8)) return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    moe_status_t st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_fp8_division_check(ctx, result));
+}
+
 moe_status_t moe_convert_probe(const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1,
                                float* e4m3_value, moe_stream_t stream) {
     if (n < 0 || n % 2 != 0) return MOE_ERR_INVALID_ARG;

@@ -408,6 +408,22 @@ moe_status_t moe_combine_partitioned(const uint16_t *partial, int64_t num_tokens
                                      uint16_t *out, int32_t *dev_status, moe_stream_t stream);
 
 /*
+ * moe_fp8_division_check -- diagnostics: the FP8 quantiser divides by its group scale with
+ * the scale's reciprocal and one correction step (after Markstein) instead of a division per
+ * element. This call checks that choice exhaustively on the GPU: for every non-negative finite
+ * bf16 amax (0 clamped to 1e-10), s = amax/448, and every bf16 x with |x| <= amax, it compares
+ * the result with the IEEE division.
+ * (No counterpart on the pages: a test hook for sglang_per_token_group_quant_fp8's x / s.)
+ *   result  [4] uint64 device out (cleared on `stream` first):
+ *           [0] pairs whose e4m3 codes differ, [1] the first one as (x bits << 32) | s bits,
+ *           [2] pairs whose quotients differ while |x / s| >= 2^-12,
+ *           [3] pairs whose quotients differ at all (expected only for |x| < 2^-103, where the
+ *               correction's remainder leaves the normal range and the code is a zero anyway).
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
+ */
+moe_status_t moe_fp8_division_check(unsigned long long *result, moe_stream_t stream);
+
+/*
  * moe_convert_probe -- diagnostics: run the number-format conversions of the quantising
  * kernels on arbitrary fp32 inputs, so their rounding, saturation, signed zeros and
  * packing order can be checked against an independent implementation of the formats.

@@ -163,3 +163,10 @@ def test_swizzled_scale_layout_validation(lib):
     assert part(H=80) == 1
     assert part(sf=ctypes.c_void_p(0x1001)) == 1
     assert part() == 0                             # no slots: nothing to launch
+
+
+def test_division_check_validation(lib):
+    f = _c(lib, "moe_fp8_division_check")
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert f(None, None) == 1
+    assert f(ctypes.c_void_p(0x1004), None) == 1      # 8-byte alignment
