@@ -129,6 +129,48 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.dtype.itemsize
+
+
+def _need(t: Optional[torch.Tensor], nbytes: int, name: str, dtype=None) -> None:
+    """Reject, before any launch, a buffer the kernels would read or write past its end (the
+    C ABI takes raw pointers and cannot see sizes) or of the wrong element type."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: {dtype} expected, got {t.dtype}")
+    if _nbytes(t) < nbytes:
+        raise ValueError(f"{name}: {nbytes} bytes needed, the tensor has {_nbytes(t)}")
+
+
+def _shape_bytes(shape, dtype) -> int:
+    n = 1
+    for d in shape:
+        n *= int(d)
+    return n * dtype.itemsize
+
+
+def _check_meta_buffers(T: int, K: int, E: int, P: int, seg_indptr, src2dst, reorder_topk_ids, masked_m,
+                        partition_counts, dev_status) -> None:
+    _need(seg_indptr, 8 * (E + 1), "seg_indptr", torch.int64)
+    _need(src2dst, 4 * T * K, "src2dst", torch.int32)
+    _need(reorder_topk_ids, 4 * T * K, "reorder_topk_ids", torch.int32)
+    _need(masked_m, 4 * E, "masked_m", torch.int32)
+    _need(partition_counts, 4 * P, "partition_counts", torch.int32)
+    _need(dev_status, 4, "dev_status", torch.int32)
+
+
+def _check_dispatch_buffers(mode: str, quant: str, T: int, H: int, K: int, E: int, M: int, out_q,
+                            out_scales) -> None:
+    qs, qd, ss, sd = dispatch_out_shapes(mode, quant, T, H, K, E, M)
+    _need(out_q, _shape_bytes(qs, qd), "out_q")
+    if ss is not None:
+        if out_scales is None:
+            raise ValueError(f"out_scales: a scale buffer is needed for quant {quant}")
+        _need(out_scales, _shape_bytes(ss, sd), "out_scales")
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         # the raw handle of torch's current stream, without building a Stream object
@@ -152,6 +194,9 @@ def moe_route_meta(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torch.T
                    partition_counts: Optional[torch.Tensor] = None, stream=None) -> int:
     """Launch moe_route_meta; returns expected_m (computed on the host)."""
     T, K = topk_ids.shape
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _check_meta_buffers(T, K, num_experts, num_partitions, seg_indptr, src2dst, reorder_topk_ids, masked_m,
+                        partition_counts, dev_status)
     em = ctypes.c_int32(0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = load_library().moe_route_meta(_ptr(topk_ids), T, K, num_experts, num_partitions, max_tokens_per_expert,
@@ -174,6 +219,9 @@ def moe_route_meta_noalloc(topk_ids: torch.Tensor, num_experts: int, seg_indptr:
     array, so calls that could overlap on the GPU must not be issued. Returns expected_m.
     """
     T, K = topk_ids.shape
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _check_meta_buffers(T, K, num_experts, num_partitions, seg_indptr, src2dst, reorder_topk_ids, masked_m,
+                        partition_counts, dev_status)
     em = ctypes.c_int32(0)
     st = load_library().moe_route_meta_noalloc(_ptr(topk_ids), T, K, num_experts, num_partitions,
                                                max_tokens_per_expert, _ptr(seg_indptr), _ptr(src2dst),
@@ -189,6 +237,11 @@ def moe_dispatch(mode: str, quant: str, hidden_states: torch.Tensor, topk_ids: t
                  max_tokens_per_expert: int = 0, input_global_scale: float = 0.0, stream=None) -> None:
     T, H = hidden_states.shape
     K = topk_ids.shape[1]
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _need(src2dst, 4 * T * K, "src2dst", torch.int32)
+    _need(seg_indptr, 8 * (num_experts + 1) if mode == "masked" else 0, "seg_indptr", torch.int64)
+    _need(dev_status, 4, "dev_status", torch.int32)
+    _check_dispatch_buffers(mode, quant, T, H, K, num_experts, max_tokens_per_expert, out_q, out_scales)
     st = load_library().moe_dispatch(MODES[mode], QUANTS[quant], _ptr(hidden_states), T, H, _ptr(topk_ids), K,
                            num_experts, max_tokens_per_expert, _ptr(src2dst), _ptr(seg_indptr),
                            float(input_global_scale), _ptr(out_q), _ptr(out_scales), _ptr(dev_status),
@@ -206,6 +259,10 @@ def moe_route_dispatch(mode: str, quant: str, hidden_states: torch.Tensor, topk_
     """moe_route_meta + moe_dispatch in one call; returns expected_m."""
     T, H = hidden_states.shape
     K = topk_ids.shape[1]
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _check_meta_buffers(T, K, num_experts, num_partitions, seg_indptr, src2dst, reorder_topk_ids, masked_m,
+                        partition_counts, dev_status)
+    _check_dispatch_buffers(mode, quant, T, H, K, num_experts, max_tokens_per_expert, out_q, out_scales)
     em = ctypes.c_int32(0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = load_library().moe_route_dispatch(
@@ -222,6 +279,14 @@ def moe_combine(mode: str, expert_out: torch.Tensor, topk_ids: torch.Tensor, top
                 dev_status: torch.Tensor, max_tokens_per_expert: int = 0, stream=None) -> None:
     T, K = topk_ids.shape
     H = out.shape[1]
+    rows = T * K if mode == "normal" else num_experts * max_tokens_per_expert
+    _need(expert_out, 2 * rows * H, "expert_out", torch.bfloat16)
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _need(topk_weights, 4 * T * K, "topk_weights", torch.float32)
+    _need(src2dst, 4 * T * K, "src2dst", torch.int32)
+    _need(seg_indptr, 8 * (num_experts + 1) if mode == "masked" else 0, "seg_indptr", torch.int64)
+    _need(out, 2 * T * H, "out", torch.bfloat16)
+    _need(dev_status, 4, "dev_status", torch.int32)
     st = load_library().moe_combine(MODES[mode], _ptr(expert_out), T, H, K, num_experts, max_tokens_per_expert,
                           _ptr(topk_ids), _ptr(src2dst), _ptr(seg_indptr), _ptr(topk_weights), _ptr(out),
                           _ptr(dev_status), _stream(stream))

@@ -1,0 +1,70 @@
+"""The Python binding rejects, before any launch, buffers that the kernels would access past
+their end or with the wrong element type (the C ABI only sees raw pointers). CPU only: the
+checks run before the binding asks for device tensors."""
+import pytest
+import torch
+
+import combine_moe_route_meta_gb300 as moe
+
+T, H, K, E, M = 16, 256, 2, 8, 8
+
+
+def _meta():
+    return dict(seg_indptr=torch.zeros(E + 1, dtype=torch.int64), src2dst=torch.zeros(T * K, dtype=torch.int32),
+                reorder_topk_ids=torch.zeros(T * K, dtype=torch.int32), masked_m=torch.zeros(E, dtype=torch.int32),
+                dev_status=torch.zeros(1, dtype=torch.int32))
+
+
+def test_route_meta_checks_sizes_and_dtypes():
+    ids = torch.zeros((T, K), dtype=torch.int32)
+    b = _meta()
+    b["seg_indptr"] = torch.zeros(E + 1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="seg_indptr"):
+        moe.moe_route_meta(ids, E, **b)
+    b = _meta()
+    b["src2dst"] = torch.zeros(T * K - 1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="src2dst"):
+        moe.moe_route_meta(ids, E, **b)
+    with pytest.raises(ValueError, match="topk_ids"):
+        moe.moe_route_meta(ids.to(torch.int64), E, **_meta())
+    b = _meta()
+    with pytest.raises(ValueError, match="partition_counts"):
+        moe.moe_route_meta(ids, E, num_partitions=4, partition_counts=torch.zeros(3, dtype=torch.int32), **b)
+
+
+def test_dispatch_checks_output_sizes():
+    x = torch.zeros((T, H), dtype=torch.bfloat16)
+    ids = torch.zeros((T, K), dtype=torch.int32)
+    s2d = torch.zeros(T * K, dtype=torch.int32)
+    seg = torch.zeros(E + 1, dtype=torch.int64)
+    st = torch.zeros(1, dtype=torch.int32)
+    q = torch.zeros((E, M, H), dtype=torch.uint8)
+    sc = torch.zeros((E, M, H // 128), dtype=torch.float32)
+    with pytest.raises(ValueError, match="out_q"):
+        moe.moe_dispatch("masked", "fp8g128", x, ids, E, s2d, seg, q[:-1], sc, st, M)
+    with pytest.raises(ValueError, match="out_scales"):
+        moe.moe_dispatch("masked", "fp8g128", x, ids, E, s2d, seg, q, None, st, M)
+    with pytest.raises(ValueError, match="out_scales"):
+        moe.moe_dispatch("masked", "fp8g128", x, ids, E, s2d, seg, q, sc[:, :-1], st, M)
+    with pytest.raises(ValueError, match="seg_indptr"):
+        moe.moe_dispatch("masked", "fp8g128", x, ids, E, s2d, seg[:-1], q, sc, st, M)
+    with pytest.raises(ValueError, match="device tensor"):     # right sizes: only the device check is left
+        moe.moe_dispatch("masked", "fp8g128", x, ids, E, s2d, seg, q, sc, st, M)
+
+
+def test_combine_checks_input_and_output_sizes():
+    ids = torch.zeros((T, K), dtype=torch.int32)
+    w = torch.zeros((T, K), dtype=torch.float32)
+    s2d = torch.zeros(T * K, dtype=torch.int32)
+    seg = torch.zeros(E + 1, dtype=torch.int64)
+    st = torch.zeros(1, dtype=torch.int32)
+    out = torch.zeros((T, H), dtype=torch.bfloat16)
+    eo_masked = torch.zeros((E * M, H), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="expert_out"):
+        moe.moe_combine("masked", eo_masked[:-1], ids, w, E, s2d, seg, out, st, M)
+    with pytest.raises(ValueError, match="topk_weights"):
+        moe.moe_combine("masked", eo_masked, ids, w.to(torch.float16), E, s2d, seg, out, st, M)
+    with pytest.raises(ValueError, match="expert_out"):
+        moe.moe_combine("normal", torch.zeros((T * K - 1, H), dtype=torch.bfloat16), ids, w, E, s2d, seg, out, st)
+    with pytest.raises(ValueError, match="device tensor"):
+        moe.moe_combine("masked", eo_masked, ids, w, E, s2d, seg, out, st, M)
