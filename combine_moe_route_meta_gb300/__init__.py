@@ -171,6 +171,43 @@ def _check_dispatch_buffers(mode: str, quant: str, T: int, H: int, K: int, E: in
         _need(out_scales, _shape_bytes(ss, sd), "out_scales")
 
 
+def _scale_bytes_ex(mode: str, quant: str, layout: str, rows: int, H: int, E: int, M: int) -> int:
+    """Bytes of moe_dispatch_ex's scale buffer for `rows` destination rows (normal layout) or
+    E x M slots (masked), in the given layout."""
+    if quant in ("none", "fp8_passthrough"):
+        return 0
+    if layout == "swizzled":
+        R = rows if mode == "normal" else E * M
+        return (R + 127) // 128 * 128 * (H // 16)
+    if quant == "nvfp4b16":
+        return (rows if mode == "normal" else E * M) * (H // 16)
+    G = H // 128
+    elem = 4 if quant == "fp8g128" else 1
+    if layout == "row":
+        return (rows if mode == "normal" else E * M) * G * elem
+    if quant == "fp8g128":                      # column-major fp32: [G, R4] (per expert in masked)
+        R4 = ((rows if mode == "normal" else M) + 3) // 4 * 4
+        return (1 if mode == "normal" else E) * G * R4 * 4
+    R4 = ((rows if mode == "normal" else M) + 3) // 4 * 4      # column-major UE8M0 words
+    return (1 if mode == "normal" else E) * ((G + 3) // 4) * R4 * 4
+
+
+def _check_partitioned_buffers(quant: str, layout: str, T: int, H: int, K: int, S: int, P: int, topk_ids,
+                               topk_weights, recv_x, recv_scales, recv_topk_ids, recv_topk_weights,
+                               dev_status) -> None:
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _need(topk_weights, 4 * T * K, "topk_weights", torch.float32)
+    _need(recv_x, P * S * (H // 2 if quant == "nvfp4b16" else 2 * H), "recv_x")
+    if quant == "nvfp4b16":
+        need = (P * S + 127) // 128 * 128 * (H // 16) if layout == "swizzled" else P * S * (H // 16)
+        if recv_scales is None:
+            raise ValueError("recv_scales: a scale buffer is needed for quant nvfp4b16")
+        _need(recv_scales, need, "recv_scales")
+    _need(recv_topk_ids, 4 * P * S * K, "recv_topk_ids", torch.int32)
+    _need(recv_topk_weights, 4 * P * S * K, "recv_topk_weights", torch.float32)
+    _need(dev_status, 4, "dev_status", torch.int32)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         # the raw handle of torch's current stream, without building a Stream object
@@ -317,6 +354,16 @@ def moe_route_meta_ex(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torc
     """moe_route_meta with expert segments aligned to ``expert_alignment`` rows and int32 or int64
     ``topk_ids`` (optionally also written as int32 to ``topk_ids_i32_out``); returns expected_m."""
     T, K = topk_ids.shape
+    E, A = num_experts, max(int(expert_alignment), 1)
+    if topk_ids.dtype not in (torch.int32, torch.int64):
+        raise ValueError(f"topk_ids: int32 or int64 expected, got {topk_ids.dtype}")
+    _need(seg_indptr, 8 * (E + 1), "seg_indptr", torch.int64)
+    _need(src2dst, 4 * T * K, "src2dst", torch.int32)
+    _need(reorder_topk_ids, 4 * (T * K + E * (A - 1)), "reorder_topk_ids", torch.int32)
+    _need(masked_m, 4 * E, "masked_m", torch.int32)
+    _need(partition_counts, 4 * num_partitions, "partition_counts", torch.int32)
+    _need(topk_ids_i32_out, 4 * T * K, "topk_ids_i32_out", torch.int32)
+    _need(dev_status, 4, "dev_status", torch.int32)
     em = ctypes.c_int32(0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = load_library().moe_route_meta_ex(_ptr(topk_ids), topk_ids.element_size(), T, K, num_experts,
@@ -334,6 +381,18 @@ def moe_dispatch_ex(mode: str, quant: str, scale_layout: str, hidden_states: tor
                     out_rows: int = 0, input_global_scale: float = 0.0, stream=None) -> None:
     T, H = hidden_states.shape
     K = topk_ids.shape[1]
+    E, M = num_experts, max_tokens_per_expert
+    rows = int(out_rows) if (mode == "normal" and out_rows) else T * K
+    row_bytes = {"none": 2 * H, "nvfp4b16": H // 2}.get(quant, H)   # passthrough: H is already bytes
+    _need(out_q, (rows if mode == "normal" else E * M) * row_bytes, "out_q")
+    need_s = _scale_bytes_ex(mode, quant, scale_layout, rows, H, E, M)
+    if need_s and out_scales is None:
+        raise ValueError(f"out_scales: a scale buffer is needed for quant {quant}")
+    _need(out_scales, need_s, "out_scales")
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _need(src2dst, 4 * T * K, "src2dst", torch.int32)
+    _need(seg_indptr, 8 * (E + 1) if mode == "masked" else 0, "seg_indptr", torch.int64)
+    _need(dev_status, 4, "dev_status", torch.int32)
     st = load_library().moe_dispatch_ex(MODES[mode], QUANTS[quant], SCALE_LAYOUTS[scale_layout], _ptr(hidden_states),
                                         T, H, _ptr(topk_ids), K, num_experts, max_tokens_per_expert, int(out_rows),
                                         _ptr(src2dst), _ptr(seg_indptr), float(input_global_scale), _ptr(out_q),
@@ -347,6 +406,17 @@ def moe_combine_ex(mode: str, expert_out: torch.Tensor, topk_ids: torch.Tensor, 
                    stream=None) -> None:
     T, K = topk_ids.shape
     H = out.shape[1]
+    if mode == "normal":
+        rows = int(expert_out_rows) if expert_out_rows else T * K
+    else:
+        rows = num_experts * max_tokens_per_expert
+    _need(expert_out, 2 * rows * H, "expert_out", torch.bfloat16)
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _need(topk_weights, 4 * T * K, "topk_weights", torch.float32)
+    _need(src2dst, 4 * T * K, "src2dst", torch.int32)
+    _need(seg_indptr, 8 * (num_experts + 1) if mode == "masked" else 0, "seg_indptr", torch.int64)
+    _need(out, 2 * T * H, "out", torch.bfloat16)
+    _need(dev_status, 4, "dev_status", torch.int32)
     st = load_library().moe_combine_ex(MODES[mode], _ptr(expert_out), T, H, K, num_experts, max_tokens_per_expert,
                                        int(expert_out_rows), _ptr(topk_ids), _ptr(src2dst), _ptr(seg_indptr),
                                        _ptr(topk_weights), _ptr(out), _ptr(dev_status), _stream(stream))
@@ -357,6 +427,11 @@ def moe_dispatch_layout(topk_ids: torch.Tensor, num_experts: int, num_partitions
                         num_tokens_per_rank: torch.Tensor, is_token_in_rank: torch.Tensor, dev_status: torch.Tensor,
                         num_tokens_per_expert: Optional[torch.Tensor] = None, stream=None) -> None:
     T, K = topk_ids.shape
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _need(num_tokens_per_rank, 4 * num_partitions, "num_tokens_per_rank", torch.int32)
+    _need(is_token_in_rank, T * num_partitions, "is_token_in_rank")
+    _need(num_tokens_per_expert, 4 * num_experts, "num_tokens_per_expert", torch.int32)
+    _need(dev_status, 4, "dev_status", torch.int32)
     st = load_library().moe_dispatch_layout(_ptr(topk_ids), T, K, num_experts, num_partitions,
                                             _ptr(num_tokens_per_rank), _ptr(is_token_in_rank),
                                             _ptr(num_tokens_per_expert), _ptr(dev_status), _stream(stream))
@@ -371,6 +446,8 @@ def moe_dispatch_partitioned(quant: str, hidden_states: torch.Tensor, topk_ids: 
     T, H = hidden_states.shape
     K = topk_ids.shape[1]
     S = recv_topk_ids.shape[1]
+    _check_partitioned_buffers(quant, "row", T, H, K, S, num_partitions, topk_ids, topk_weights, recv_x,
+                               recv_scales, recv_topk_ids, recv_topk_weights, dev_status)
     st = load_library().moe_dispatch_partitioned(
         QUANTS[quant], _ptr(hidden_states), T, S, H, _ptr(topk_ids), _ptr(topk_weights), K, num_experts,
         num_partitions, int(invalid_expert_id), float(input_global_scale), _ptr(recv_x), _ptr(recv_scales),
@@ -386,6 +463,8 @@ def moe_dispatch_partitioned_ex(quant: str, scale_layout: str, hidden_states: to
     T, H = hidden_states.shape
     K = topk_ids.shape[1]
     S = recv_topk_ids.shape[1]
+    _check_partitioned_buffers(quant, scale_layout, T, H, K, S, num_partitions, topk_ids, topk_weights, recv_x,
+                               recv_scales, recv_topk_ids, recv_topk_weights, dev_status)
     st = load_library().moe_dispatch_partitioned_ex(
         QUANTS[quant], SCALE_LAYOUTS[scale_layout], _ptr(hidden_states), T, S, H, _ptr(topk_ids), _ptr(topk_weights),
         K, num_experts, num_partitions, int(invalid_expert_id), float(input_global_scale), _ptr(recv_x),
@@ -402,6 +481,10 @@ def moe_combine_partitioned(partial: torch.Tensor, topk_ids: torch.Tensor, num_e
                             out: torch.Tensor, dev_status: torch.Tensor, stream=None) -> None:
     T, K = topk_ids.shape
     _, S, H = partial.shape
+    _need(partial, num_partitions * S * H * 2, "partial", torch.bfloat16)
+    _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
+    _need(out, 2 * T * H, "out", torch.bfloat16)
+    _need(dev_status, 4, "dev_status", torch.int32)
     st = load_library().moe_combine_partitioned(_ptr(partial), T, S, H, _ptr(topk_ids), K, num_experts,
                                                 num_partitions, _ptr(out), _ptr(dev_status), _stream(stream))
     _check(st, "moe_combine_partitioned")

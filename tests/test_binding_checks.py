@@ -68,3 +68,39 @@ def test_combine_checks_input_and_output_sizes():
         moe.moe_combine("normal", torch.zeros((T * K - 1, H), dtype=torch.bfloat16), ids, w, E, s2d, seg, out, st)
     with pytest.raises(ValueError, match="device tensor"):
         moe.moe_combine("masked", eo_masked, ids, w, E, s2d, seg, out, st, M)
+
+
+def test_ex_and_partitioned_wrappers_check_sizes():
+    x = torch.zeros((T, H), dtype=torch.bfloat16)
+    ids = torch.zeros((T, K), dtype=torch.int32)
+    w = torch.zeros((T, K), dtype=torch.float32)
+    s2d = torch.zeros(T * K, dtype=torch.int32)
+    seg = torch.zeros(E + 1, dtype=torch.int64)
+    st = torch.zeros(1, dtype=torch.int32)
+    cap = T * K + 5
+    q = torch.zeros((cap, H), dtype=torch.uint8)
+    G, R4 = H // 128, (cap + 3) // 4 * 4
+    col = torch.zeros((G, R4), dtype=torch.float32)
+    with pytest.raises(ValueError, match="out_scales"):        # column-major needs R4 = roundup(out_rows, 4)
+        moe.moe_dispatch_ex("normal", "fp8g128", "col", x, ids, E, s2d, seg, q, col[:, :-4], st, out_rows=cap)
+    with pytest.raises(ValueError, match="out_q"):
+        moe.moe_dispatch_ex("normal", "fp8g128", "col", x, ids, E, s2d, seg, q[:-1], col, st, out_rows=cap)
+    sw = torch.zeros(moe.swizzled_scale_bytes(T * K, H) - 1, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="out_scales"):
+        moe.moe_dispatch_ex("normal", "nvfp4b16", "swizzled", x, ids, E, s2d, seg,
+                            torch.zeros((T * K, H // 2), dtype=torch.uint8), sw, st)
+    with pytest.raises(ValueError, match="reorder_topk_ids"):  # alignment padding rows need room
+        moe.moe_route_meta_ex(ids, E, seg, s2d, torch.zeros(T * K, dtype=torch.int32),
+                              torch.zeros(E, dtype=torch.int32), st, expert_alignment=4)
+    P, S = 2, T
+    rx = torch.zeros((P, S, H // 2), dtype=torch.uint8)
+    rsf = torch.zeros((P, S, H // 16), dtype=torch.uint8)
+    rids = torch.zeros((P, S, K), dtype=torch.int32)
+    rw = torch.zeros((P, S, K), dtype=torch.float32)
+    with pytest.raises(ValueError, match="recv_scales"):       # swizzled: rows padded to 128
+        moe.moe_dispatch_partitioned_ex("nvfp4b16", "swizzled", x, ids, w, E, P, rx, rsf, rids, rw, st)
+    with pytest.raises(ValueError, match="recv_x"):
+        moe.moe_dispatch_partitioned("nvfp4b16", x, ids, w, E, P, rx[:1], rsf, rids, rw, st)
+    with pytest.raises(ValueError, match="partial"):
+        moe.moe_combine_partitioned(torch.zeros((1, S, H), dtype=torch.bfloat16), ids, E, P,
+                                    torch.zeros((T, H), dtype=torch.bfloat16), st)
