@@ -735,7 +735,9 @@ def run_gpu(args, w, rank, world, dist):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy PCG64 inputs, random expert outputs)",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy PCG64 inputs, random expert outputs)",
+        "dtypes": "f32 arithmetic (quantiser, combine accumulation) on bf16 rows; fp8 / nvfp4 / bf16 rows out; "
+                  "int32 metadata",
         "ms_per_step_median": ms_median,
         "ms_per_step_with_kernel_events": ms_k,
         "graph_replay": graph_replay,

@@ -81,6 +81,13 @@ def test_qwen3_masked_secondary():
     (1100, 2048, 32, 6, "masked", "nvfp4b16", 400),
     (1030, 512, 16, 4, "masked", "none", 500),
     (2048, 4096, 128, 8, "normal", "none", 0),
+    # other models' hidden sizes: 16384 (32 slices, so warps loop), 5120, 2880 (ragged slice)
+    (96, 16384, 64, 4, "normal", "fp8g128", 0),
+    (1100, 16384, 64, 4, "masked", "nvfp4b16", 200),
+    (300, 5120, 160, 6, "normal", "fp8g128", 0),
+    (1024, 5120, 160, 6, "masked", "fp8g128", 64),
+    (200, 2880, 32, 4, "normal", "none", 0),
+    (1100, 2880, 32, 4, "masked", "nvfp4b16", 300),
 ])
 def test_shapes_full(T, H, E, K, mode, quant, M):
     w = make_case(T, H, E, K, seed=T + H + E + K, mode=mode, quant=quant, M=M, invalid_rate=0.05)
@@ -253,6 +260,8 @@ def test_dispatcher_graph_capture_replays_correctly(case):
 # --- moe_route_dispatch: route + dispatch in one call -------------------------------------
 
 @pytest.mark.parametrize("T,H,E,K,mode,quant,M,P", [
+    (64, 16384, 64, 4, "masked", "fp8g128", 64, 4),     # 32 slices per token: warps loop
+    (100, 2880, 32, 4, "normal", "nvfp4b16", 0, 2),     # ragged last slice
     (128, 7168, 256, 8, "masked", "fp8g128", 128, 8),   # the decode shape: one fused kernel
     (1, 16, 1, 1, "normal", "none", 0, 1),
     (33, 272, 5, 3, "masked", "none", 9, 5),             # capacity drops inside the fused kernel
