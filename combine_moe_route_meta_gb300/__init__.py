@@ -163,12 +163,16 @@ def _check_meta_buffers(T: int, K: int, E: int, P: int, seg_indptr, src2dst, reo
 
 def _check_dispatch_buffers(mode: str, quant: str, T: int, H: int, K: int, E: int, M: int, out_q,
                             out_scales) -> None:
+    """The masked layout fixes the output size ([E, M, .]); the contiguous layout needs
+    N = seg_indptr[E] rows, known only on the device, so only the scale buffer's presence is
+    checked there."""
     qs, qd, ss, sd = dispatch_out_shapes(mode, quant, T, H, K, E, M)
-    _need(out_q, _shape_bytes(qs, qd), "out_q")
-    if ss is not None:
-        if out_scales is None:
-            raise ValueError(f"out_scales: a scale buffer is needed for quant {quant}")
-        _need(out_scales, _shape_bytes(ss, sd), "out_scales")
+    if ss is not None and out_scales is None:
+        raise ValueError(f"out_scales: a scale buffer is needed for quant {quant}")
+    if mode == "masked":
+        _need(out_q, _shape_bytes(qs, qd), "out_q")
+        if ss is not None:
+            _need(out_scales, _shape_bytes(ss, sd), "out_scales")
 
 
 def _scale_bytes_ex(mode: str, quant: str, layout: str, rows: int, H: int, E: int, M: int) -> int:
@@ -316,7 +320,8 @@ def moe_combine(mode: str, expert_out: torch.Tensor, topk_ids: torch.Tensor, top
                 dev_status: torch.Tensor, max_tokens_per_expert: int = 0, stream=None) -> None:
     T, K = topk_ids.shape
     H = out.shape[1]
-    rows = T * K if mode == "normal" else num_experts * max_tokens_per_expert
+    # the contiguous layout reads N = seg_indptr[E] rows (known only on the device)
+    rows = 0 if mode == "normal" else num_experts * max_tokens_per_expert
     _need(expert_out, 2 * rows * H, "expert_out", torch.bfloat16)
     _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
     _need(topk_weights, 4 * T * K, "topk_weights", torch.float32)
@@ -384,11 +389,14 @@ def moe_dispatch_ex(mode: str, quant: str, scale_layout: str, hidden_states: tor
     E, M = num_experts, max_tokens_per_expert
     rows = int(out_rows) if (mode == "normal" and out_rows) else T * K
     row_bytes = {"none": 2 * H, "nvfp4b16": H // 2}.get(quant, H)   # passthrough: H is already bytes
-    _need(out_q, (rows if mode == "normal" else E * M) * row_bytes, "out_q")
+    # sizes are fixed by the masked layout, by a declared out_rows, or (swizzled scales) by
+    # the row count the tile layout is built over; otherwise N rows, known only on the device
+    declared = mode == "masked" or bool(out_rows)
+    _need(out_q, (rows if mode == "normal" else E * M) * row_bytes if declared else 0, "out_q")
     need_s = _scale_bytes_ex(mode, quant, scale_layout, rows, H, E, M)
     if need_s and out_scales is None:
         raise ValueError(f"out_scales: a scale buffer is needed for quant {quant}")
-    _need(out_scales, need_s, "out_scales")
+    _need(out_scales, need_s if (declared or scale_layout == "swizzled") else 0, "out_scales")
     _need(topk_ids, 4 * T * K, "topk_ids", torch.int32)
     _need(src2dst, 4 * T * K, "src2dst", torch.int32)
     _need(seg_indptr, 8 * (E + 1) if mode == "masked" else 0, "seg_indptr", torch.int64)
@@ -407,7 +415,7 @@ def moe_combine_ex(mode: str, expert_out: torch.Tensor, topk_ids: torch.Tensor, 
     T, K = topk_ids.shape
     H = out.shape[1]
     if mode == "normal":
-        rows = int(expert_out_rows) if expert_out_rows else T * K
+        rows = int(expert_out_rows)   # a declared capacity; 0: N rows, known only on the device
     else:
         rows = num_experts * max_tokens_per_expert
     _need(expert_out, 2 * rows * H, "expert_out", torch.bfloat16)

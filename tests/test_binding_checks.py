@@ -64,10 +64,15 @@ def test_combine_checks_input_and_output_sizes():
         moe.moe_combine("masked", eo_masked[:-1], ids, w, E, s2d, seg, out, st, M)
     with pytest.raises(ValueError, match="topk_weights"):
         moe.moe_combine("masked", eo_masked, ids, w.to(torch.float16), E, s2d, seg, out, st, M)
-    with pytest.raises(ValueError, match="expert_out"):
-        moe.moe_combine("normal", torch.zeros((T * K - 1, H), dtype=torch.bfloat16), ids, w, E, s2d, seg, out, st)
     with pytest.raises(ValueError, match="device tensor"):
         moe.moe_combine("masked", eo_masked, ids, w, E, s2d, seg, out, st, M)
+    # the contiguous layout reads N = seg_indptr[E] rows, which only the device knows: a
+    # compact buffer of fewer than T*K rows is legal and passes to the device check
+    with pytest.raises(ValueError, match="device tensor"):
+        moe.moe_combine("normal", torch.zeros((T * K - 3, H), dtype=torch.bfloat16), ids, w, E, s2d, seg, out, st)
+    with pytest.raises(ValueError, match="expert_out"):
+        moe.moe_combine_ex("normal", torch.zeros((T * K - 3, H), dtype=torch.bfloat16), ids, w, E, s2d, seg, out,
+                           st, expert_out_rows=T * K)
 
 
 def test_ex_and_partitioned_wrappers_check_sizes():
