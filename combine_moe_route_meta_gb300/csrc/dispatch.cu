@@ -345,7 +345,11 @@ cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkG
         return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
     } else {
         auto kern = dispatch_bulk_quant_kernel<QUANT, MASKED>;
-        threads = kBulkQuantThreads;
+        // as many passes over the row's 16-element slices as 256 threads need, with the block
+        // sized so that every pass is full (H = 7168: 448 slices = 2 x 224, not 256 + 192)
+        const int nslices = a.H / kLaneElems;
+        const int passes = (nslices + kBulkQuantThreads - 1) / kBulkQuantThreads;
+        threads = ((nslices + passes - 1) / passes + 31) / 32 * 32;
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err == cudaSuccess) err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
         if (err != cudaSuccess) return err;
