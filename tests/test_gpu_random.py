@@ -32,7 +32,7 @@ def _random_case(seed):
                      bad_rate=float(rng.choice([0.0, 0.0, 0.01])), routing=routing), quant
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(40))
 def test_random_configurations(seed):
     w, quant = _random_case(seed)
     if quant != "fp8g128_ue8m0":
@@ -68,3 +68,57 @@ def test_random_configurations(seed):
         assert np.array_equal(gq[r], q) and np.array_equal(gs[r], e)
         written[r] = True
     assert (gq[~written] == SENTINEL).all()
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_partitioned_layouts(seed):
+    """The FlashInfer one-row-per-partition layout and its combine on seeded random shapes,
+    against the oracle in full (bf16 or NVFP4 payload, row-major or swizzled scales)."""
+    rng = np.random.default_rng(5000 + seed)
+    quant = "nvfp4b16" if seed % 2 else "none"
+    layout = "swizzled" if seed % 4 == 1 else "row"
+    P = int(rng.choice([1, 2, 4, 8, 16, 32]))
+    E = P * int(rng.integers(1, 9))
+    K = int(rng.integers(1, min(16, E) + 1))
+    H = int(rng.integers(1, 20)) * 64
+    T = int(rng.integers(0, 1500))
+    S = T + int(rng.integers(0, 40))
+    w = make_case(T, H, E, K, seed=seed, quant=quant, invalid_rate=float(rng.choice([0.0, 0.1])),
+                  routing="uniform" if K <= E else "replace")
+    m = moe()
+    x, ids, wt = to_dev(w)
+    g = w.global_scale or 0.0
+    inv = int(rng.choice([-1, E]))
+    if quant == "nvfp4b16":
+        rx = filled((P, S, H // 2), torch.uint8)
+        rsf = filled((m.swizzled_scale_bytes(P * S, H),) if layout == "swizzled" else (P, S, H // 16), torch.uint8)
+    else:
+        rx = filled((P, S, H), torch.bfloat16)
+        rsf = None
+    rids = filled((P, S, K), torch.int32)
+    rw = filled((P, S, K), torch.float32)
+    st = m.new_status()
+    if S:
+        m.moe_dispatch_partitioned_ex(quant, layout, x, ids, wt, E, P, rx, rsf, rids, rw, st, invalid_expert_id=inv,
+                                      input_global_scale=g)
+    ox, osf, oids, ow = oracle.dispatch_partitioned(quant, w.x, w.topk_ids, w.topk_weights, E, P, invalid_id=inv,
+                                                    global_scale=g, num_slots=S, fill=SENTINEL)
+    torch.cuda.synchronize()
+    assert np.array_equal(bytes_of(rx).reshape(-1), np.ascontiguousarray(ox).view(np.uint8).reshape(-1))
+    if rsf is not None:
+        want = oracle.nvfp4_sf_interleave(osf.reshape(P * S, H // 16)) if layout == "swizzled" else osf.reshape(-1)
+        assert np.array_equal(rsf.cpu().numpy().reshape(-1), want.reshape(-1))
+    assert np.array_equal(rids.cpu().numpy(), oids)
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
+    assert int(st.item()) == 0
+    if T == 0:
+        return
+    from workloads import random_bf16
+    from _harness import check_combine
+    partial_h = random_bf16(np.random.default_rng(seed + 77), (P, S, H))
+    partial = torch.from_numpy(partial_h.view(np.int16)).cuda().view(torch.bfloat16)
+    out = filled((T, H), torch.bfloat16)
+    m.moe_combine_partitioned(partial, ids, E, P, out, st)
+    want = oracle.combine_partitioned(partial_h, w.topk_ids, E, P)
+    torch.cuda.synchronize()
+    check_combine(bytes_of(out).view(np.uint16).reshape(T, H), want)
