@@ -86,6 +86,8 @@ cudaError_t blocks_per_sm(const LaunchCtx& ctx, Kernel kern, int threads, size_t
 // thread block. One block handles everything when n_pairs <= kRouteSingleMax.
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteRMax = 16;
+// one block up to 8192 pairs (8 rounds per warp): at 32768 pairs one block took 48.5 us
+// against 12.7 us for the count + place kernels (measured, prefill shape)
 constexpr int64_t kRouteSingleMax = 8192;
 constexpr int kRouteTargetBlocks = 128;
 

@@ -137,14 +137,20 @@ __device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, cons
     const unsigned lt = (1u << lane) - 1u;
     int* my = cnt + w * cnt_stride(E);
     bool bad = false;
+    // all of this lane's ids first, in one batch of loads (er[r] holds the raw id until
+    // round r replaces it with the packed expert and rank)
 #pragma unroll
     for (int r = 0; r < RMAX; r++) {
-        er[r] = pack_er(-1, 0);
+        const int64_t i = warp_base + r * 32 + lane;
+        er[r] = (r < R && i < n_pairs) ? read_id(ids, ids64, i) : -1;
+    }
+#pragma unroll
+    for (int r = 0; r < RMAX; r++) {
         if (r < R) {
             const int64_t i = warp_base + r * 32 + lane;
-            int e = -1;
+            int e = er[r];
+            er[r] = pack_er(-1, 0);
             if (i < n_pairs) {
-                e = read_id(ids, ids64, i);
                 if (ids_out != nullptr) ids_out[i] = e;
                 if (e < -1 || e >= E) {
                     bad = true;
@@ -159,6 +165,8 @@ __device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, cons
             if (e >= 0 && lane == __ffs(peers) - 1) my[e] = base + __popc(peers);
             __syncwarp();
             er[r] = pack_er(e, base + __popc(peers & lt));
+        } else {
+            er[r] = pack_er(-1, 0);
         }
     }
     if (__any_sync(kFullMask, bad) && lane == 0) set_status(status, MOE_ERR_BAD_EXPERT_ID);
@@ -362,16 +370,20 @@ __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteAr
 }
 
 template <int RMAX>
+cudaError_t launch_single(const LaunchCtx& ctx, const RouteArgs& a, int E) {
+    const size_t smem = route_smem_bytes(E);
+    auto k = route_meta_single_kernel<RMAX>;
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (err != cudaSuccess) return err;
+    }
+    return launch_pdl(ctx, k, dim3(1), dim3(kRouteThreads), smem, a);
+}
+
+template <int RMAX>
 cudaError_t launch_rmax(const LaunchCtx& ctx, const RoutePlan& plan, const RouteArgs& a, int E) {
     const size_t smem = route_smem_bytes(E);
-    if (plan.single) {
-        auto k = route_meta_single_kernel<RMAX>;
-        if (smem > 48 * 1024) {
-            cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-            if (err != cudaSuccess) return err;
-        }
-        return launch_pdl(ctx, k, dim3(1), dim3(kRouteThreads), smem, a);
-    }
+    if (plan.single) return launch_single<RMAX>(ctx, a, E);
     auto k1 = route_meta_count_kernel<RMAX>;
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
