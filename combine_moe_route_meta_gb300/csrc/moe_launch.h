@@ -86,9 +86,10 @@ cudaError_t blocks_per_sm(const LaunchCtx& ctx, Kernel kern, int threads, size_t
 // thread block. One block handles everything when n_pairs <= kRouteSingleMax.
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteRMax = 16;
-// one block up to 8192 pairs (8 rounds per warp): at 32768 pairs one block took 48.5 us
-// against 12.7 us for the count + place kernels (measured, prefill shape)
-constexpr int64_t kRouteSingleMax = 8192;
+// one block up to 2048 pairs (2 rounds per warp). Measured after an L2 flush: one block
+// 8.5 / 10.2 / 11.3 / 14.3 / 18.4 us at 256 / 1024 / 2048 / 4096 / 8192 pairs, the count +
+// place kernels 11.3 / 12.8 / 12.8 / 12.9 / 13.3 us.
+constexpr int64_t kRouteSingleMax = 2048;
 constexpr int kRouteTargetBlocks = 128;
 
 struct RoutePlan {

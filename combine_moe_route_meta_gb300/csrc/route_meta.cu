@@ -17,7 +17,7 @@
 //    Walking rounds in order keeps the rank stable (flattened order).
 //  * A per-expert exclusive scan over the 32 warp counters turns warp ranks into
 //    block ranks and gives the block's histogram.
-//  * One block (n_pairs <= 8192): block-wide scan of the histogram -> seg_indptr, and
+//  * One block (n_pairs <= 2048): block-wide scan of the histogram -> seg_indptr, and
 //    the final positions are written in the same kernel.
 //  * Several blocks: each block publishes its histogram row to a [B][E] table and writes
 //    block ranks into src2dst. A second kernel (launched as a programmatic dependent)

@@ -195,7 +195,7 @@ moe_status_t moe_route_meta_ex(const void *topk_ids, int topk_ids_bytes, int64_t
  * the library holds it until the process exits). Sizes whose moe_route_meta workspace
  * would exceed 1 MiB are rejected with MOE_ERR_UNSUPPORTED before anything is launched:
  * with 1024 experts it covers up to 4,177,920 (token, k) pairs, with 256 experts up to
- * 16,760,832. Up to 8192 pairs need no scratch at all.
+ * 16,760,832. Up to 2048 pairs need no scratch at all.
  * First call on a device: looks up the array's device address with that device current;
  * make that first call before any stream capture. Each call clears the scratch header
  * with a cudaMemsetAsync on `stream` before its kernels.

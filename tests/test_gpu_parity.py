@@ -110,12 +110,13 @@ def test_large_route_meta_many_rounds():
     (400000, 8, 256, "uniform"),  # 196 blocks of 16 rounds (more than one wave)
     (20000, 8, 1024, "zipf"),     # 79 blocks of 2 rounds, E = 1024: the largest shared-memory footprint
     (9000, 1, 7, "uniform"),      # 9 blocks, odd E smaller than a warp
-    (1024, 8, 256, "zipf"),       # 8192 pairs: the largest one-block case, 8 rounds per warp
-    (1025, 8, 256, "zipf"),       # one token more: count + place over 9 blocks
-    (1000, 8, 1024, "uniform"),   # 8000 pairs with E = 1024 in one block
+    (256, 8, 256, "zipf"),        # 2048 pairs: the largest one-block case, 2 rounds per warp
+    (257, 8, 256, "zipf"),        # one token more: count + place over 3 blocks
+    (250, 8, 1024, "uniform"),    # 2000 pairs with E = 1024 in one block
+    (1024, 8, 256, "zipf"),       # 8192 pairs: count + place over 8 blocks
 ])
 def test_multi_block_route_meta_paths(T, K, E, routing):
-    """Metadata in full across the size classes: one block up to 8192 pairs, then the count
+    """Metadata in full across the size classes: one block up to 2048 pairs, then the count
     and place kernels (up to more blocks than fit on the GPU at once); the workspace is
     reused across calls."""
     w = make_case(T, 16, E, K, seed=T + E, routing=routing, invalid_rate=0.03)
