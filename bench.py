@@ -582,7 +582,7 @@ def run_gpu(args, w, rank, world, dist):
     stream = torch.cuda.current_stream()
     route_launches = 1 if moe.moe_route_meta_workspace_size(w.T, w.K, w.E) == 0 else 2
     # small batches: route + dispatch as one fused kernel (moe_route_dispatch)
-    fused = not args.no_fuse and w.T <= 1024 and w.T * w.K <= 4096
+    fused = not args.no_fuse and w.T <= 512 and w.T * w.K <= 4096
 
     def step():
         if fused:

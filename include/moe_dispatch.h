@@ -289,7 +289,7 @@ moe_status_t moe_dispatch_ex(moe_mode_t mode, moe_quant_t quant, moe_scale_layou
  * one step). Arguments are the union of the two calls' arguments, with the same meaning
  * and limits; max_tokens_per_expert is the masked capacity (>= 1 in masked mode; >= 0 in
  * normal mode, where M > 0 only enables the capacity check of masked_m).
- * Small batches (T <= 1024 and T*K <= 4096 pairs) run as a single kernel that needs no
+ * Small batches (T <= 512 and T*K <= 4096 pairs) run as a single kernel that needs no
  * workspace (workspace may be NULL); larger ones need moe_route_meta_workspace_size(T, K, E)
  * bytes of zero-filled workspace, exactly as moe_route_meta.
  * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.

@@ -272,7 +272,8 @@ def test_dispatcher_graph_capture_replays_correctly(case):
     (33, 272, 5, 3, "masked", "none", 9, 5),             # capacity drops inside the fused kernel
     (100, 1040, 64, 6, "normal", "nvfp4b16", 0, 4),
     (256, 4096, 128, 16, "masked", "nvfp4b16", 64, 8),   # 4096 pairs: the largest fused batch
-    (1024, 128, 1024, 4, "normal", "fp8g128", 0, 2),     # 1024 tokens, E at its limit
+    (512, 256, 64, 2, "normal", "fp8g128", 0, 2),        # 512 tokens: the largest fused batch by tokens
+    (1024, 128, 1024, 4, "normal", "fp8g128", 0, 2),     # 1024 tokens (past the fused limit), E at its limit
     (4096, 512, 256, 8, "normal", "fp8g128", 0, 8),      # beyond the fused limits: route kernels + dispatch
     (513, 256, 16, 8, "masked", "none", 600, 4),         # 4104 pairs: just past the fused limit
 ])
