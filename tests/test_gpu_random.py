@@ -1,6 +1,12 @@
 """Randomised GPU parity: seeded random shapes, modes, quantisations, routing skew,
 invalid/out-of-range slots and duplicate experts, each run through route_meta, dispatch
-and combine (and the fused route_dispatch) and compared with the oracle in full."""
+and combine (and the fused route_dispatch) and compared with the oracle in full; the
+one-row-per-partition layout; expert-aligned metadata from int32 or int64 ids.
+
+MOE_RANDOM_SEEDS (default 40) sets the number of full-path seeds; the partitioned and the
+aligned-metadata tests run a quarter and three quarters as many (at least 10 and 30)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -13,6 +19,7 @@ from _harness import SENTINEL, bytes_of, check_meta, filled, moe, run_full, to_d
 pytestmark = pytest.mark.gpu
 
 QUANTS = ["none", "fp8g128", "nvfp4b16", "fp8g128_ue8m0"]
+N_SEEDS = max(1, int(os.environ.get("MOE_RANDOM_SEEDS", "40")))
 
 
 def _random_case(seed):
@@ -32,7 +39,7 @@ def _random_case(seed):
                      bad_rate=float(rng.choice([0.0, 0.0, 0.01])), routing=routing), quant
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(N_SEEDS))
 def test_random_configurations(seed):
     w, quant = _random_case(seed)
     if quant != "fp8g128_ue8m0":
@@ -70,7 +77,7 @@ def test_random_configurations(seed):
     assert (gq[~written] == SENTINEL).all()
 
 
-@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("seed", range(max(10, N_SEEDS // 4)))
 def test_random_partitioned_layouts(seed):
     """The FlashInfer one-row-per-partition layout and its combine on seeded random shapes,
     against the oracle in full (bf16 or NVFP4 payload, row-major or swizzled scales)."""
@@ -122,3 +129,47 @@ def test_random_partitioned_layouts(seed):
     want = oracle.combine_partitioned(partial_h, w.topk_ids, E, P)
     torch.cuda.synchronize()
     check_combine(bytes_of(out).view(np.uint16).reshape(T, H), want)
+
+
+@pytest.mark.parametrize("seed", range(max(30, 3 * N_SEEDS // 4)))
+def test_random_aligned_route_meta(seed):
+    """moe_route_meta_ex on seeded random shapes: expert alignment A in {1, 2, 8, 128, 1024},
+    int32 or int64 ids (with the int32 copy), partitions, capacity checks, invalid and
+    out-of-range ids; every output against the oracle, the padding tail of
+    reorder_topk_ids untouched."""
+    rng = np.random.default_rng(9000 + seed)
+    m = moe()
+    P = int(rng.choice([1, 2, 4, 8]))
+    E = min(P * int(rng.integers(1, 129)), 1024)
+    K = int(rng.integers(1, min(16, E) + 1))
+    T = int(rng.integers(0, 6000)) if seed % 3 else int(rng.integers(0, 300))
+    A = int(rng.choice([1, 2, 8, 128, 1024]))
+    M = int(rng.integers(0, max(2, 2 * T * K // E + 2)))
+    w = make_case(T, 16, E, K, seed=seed, routing="zipf" if seed % 2 else "uniform",
+                  invalid_rate=float(rng.choice([0.0, 0.05])), bad_rate=float(rng.choice([0.0, 0.01])))
+    use64 = seed % 2 == 0
+    ids = torch.from_numpy(np.ascontiguousarray(w.topk_ids.astype(np.int64) if use64 else w.topk_ids)).cuda()
+    cap = T * K + E * (A - 1)
+    seg = filled((E + 1,), torch.int64)
+    s2d = filled((T * K,), torch.int32)
+    reo = filled((cap,), torch.int32)
+    mm = filled((E,), torch.int32)
+    pc = filled((P,), torch.int32)
+    i32 = filled((T, K), torch.int32) if use64 else None
+    st = m.new_status()
+    em = m.moe_route_meta_ex(ids, E, seg, s2d, reo, mm, st, m.new_workspace(T, K, E), P, M, A, pc,
+                             topk_ids_i32_out=i32)
+    om = oracle.route_meta_aligned(w.topk_ids, E, A, P=P, M=M)
+    torch.cuda.synchronize()
+    n = int(om.seg_indptr[-1])
+    assert np.array_equal(seg.cpu().numpy(), om.seg_indptr)
+    assert np.array_equal(s2d.cpu().numpy(), om.src2dst)
+    assert np.array_equal(reo[:n].cpu().numpy(), om.reorder_topk_ids)
+    assert (bytes_of(reo[n:]) == SENTINEL).all()
+    assert np.array_equal(mm.cpu().numpy(), om.masked_m)
+    assert np.array_equal(pc.cpu().numpy(), om.partition_counts)
+    assert em == om.expected_m
+    if use64:
+        assert np.array_equal(i32.cpu().numpy(), w.topk_ids)
+    # first error wins on the GPU: with both a bad id and an overflow either code may land
+    assert (int(st.item()) == 0) == (om.status == 0)
