@@ -66,6 +66,7 @@ _SIGNATURES = {
     "moe_combine": (_int, [_int, _P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P]),
     "moe_convert_probe": (_int, [_P, _i64, _P, _P, _P, _P]),
     "moe_fp8_division_check": (_int, [_P, _P]),
+    "moe_wait_timeout_check": (_int, [_P, _i64, _int, _P]),
     "moe_route_meta_noalloc": (_int, [_P, _i64, _int, _int, _int, _int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_route_dispatch": (_int, [_int, _int, _P, _i64, _int, _P, _int, _int, _int, _int, _f32, _P, _P, _P, _P,
                                   _P, _P, _P, _sz, _P, _P, _P, _P]),
@@ -348,6 +349,16 @@ def moe_fp8_division_check(result: torch.Tensor, stream=None) -> None:
     division against the IEEE division over its whole input domain."""
     st = load_library().moe_fp8_division_check(_ptr(result), _stream(stream))
     _check(st, "moe_fp8_division_check")
+
+
+def moe_wait_timeout_check(dev_status: torch.Tensor, limit_ns: int, complete: bool, stream=None) -> None:
+    """Diagnostics: the bulk dispatch kernels' bounded mbarrier wait on a barrier that is
+    completed first (complete=True: dev_status stays MOE_OK) or never (complete=False: the
+    wait gives up after limit_ns and dev_status becomes MOE_ERR_TIMEOUT)."""
+    _need(dev_status, 4, "dev_status", torch.int32)
+    st = load_library().moe_wait_timeout_check(_ptr(dev_status), int(limit_ns), 1 if complete else 0,
+                                               _stream(stream))
+    _check(st, "moe_wait_timeout_check")
 
 
 def moe_route_meta_ex(topk_ids: torch.Tensor, num_experts: int, seg_indptr: torch.Tensor, src2dst: torch.Tensor,

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
     if (lane == 0) {
         bulk_wait_all();
         // after a timeout, loads still in flight are waited for (bounded) before shared memory is released
-        for (int64_t j = consumed; j < issued; j++) mbar_wait(bar0 + 8 * int(j % NS), uint32_t((j / NS) & 1), 1 << 20);
+        for (int64_t j = consumed; j < issued; j++) mbar_wait(bar0 + 8 * int(j % NS), uint32_t((j / NS) & 1), kDrainLimitNs);
     }
 }
 
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
     if (tid == 0) {
         bulk_wait_all();
         // after a timeout, loads still in flight are waited for (bounded) before shared memory is released
-        for (int64_t j = consumed; j < issued; j++) mbar_wait(bar0 + 8 * int(j % NS), uint32_t((j / NS) & 1), 1 << 20);
+        for (int64_t j = consumed; j < issued; j++) mbar_wait(bar0 + 8 * int(j % NS), uint32_t((j / NS) & 1), kDrainLimitNs);
     }
 }
 
@@ -430,6 +430,22 @@ __global__ void __launch_bounds__(256) fp8_division_check_kernel(unsigned long l
             }
         }
     }
+}
+
+// The bulk kernels' bounded ring wait on one mbarrier of count 1: arrived at first
+// (complete = 1), or never arrived at (complete = 0), when the wait has to give up.
+__global__ void wait_timeout_check_kernel(int32_t* status, uint64_t limit_ns, int complete) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    mbar_fence_init();
+    if (complete) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
+    if (!mbar_wait(b, 0, limit_ns)) set_status(status, MOE_ERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout_check(const LaunchCtx& ctx, int32_t* status, uint64_t limit_ns, int complete) {
+    wait_timeout_check_kernel<<<1, 1, 0, ctx.stream>>>(status, limit_ns, complete);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_fp8_division_check(const LaunchCtx& ctx, unsigned long long* result) {

@@ -405,6 +405,15 @@ moe_status_t moe_fp8_division_check(unsigned long long* result, moe_stream_t str
     return from_cuda(moe::launch_fp8_division_check(ctx, result));
 }
 
+moe_status_t moe_wait_timeout_check(int32_t* dev_status, int64_t limit_ns, int complete, moe_stream_t stream) {
+    if (!dev_status || !aligned(dev_status, 4)) return MOE_ERR_INVALID_ARG;
+    if (limit_ns <= 0 || limit_ns > 10000000000ll || (complete != 0 && complete != 1)) return MOE_ERR_INVALID_ARG;
+    moe::LaunchCtx ctx;
+    moe_status_t st = make_ctx(stream, &ctx);
+    if (st != MOE_OK) return st;
+    return from_cuda(moe::launch_wait_timeout_check(ctx, dev_status, uint64_t(limit_ns), complete));
+}
+
 moe_status_t moe_convert_probe(const float* in, int64_t n, uint8_t* e4m3, uint8_t* e2m1,
                                float* e4m3_value, moe_stream_t stream) {
     if (n < 0 || n % 2 != 0) return MOE_ERR_INVALID_ARG;

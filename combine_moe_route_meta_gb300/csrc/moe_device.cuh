@@ -156,21 +156,47 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // generic-proxy shared-memory writes become visible to later bulk copies
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Bounded wait for phase `parity` of an mbarrier: false after `limit` polls (the caller
-// reports MOE_ERR_TIMEOUT instead of hanging).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int limit = 1 << 24) {
-    for (int it = 0; it < limit; it++) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
+// Global nanosecond clock (%globaltimer).
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One test of phase `parity` of an mbarrier (the thread may be suspended for a short,
+// hardware-defined time while the phase is pending).
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Limits of the bounded waits: a bulk row load normally lands within microseconds.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // ring waits: 1 s
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // draining loads after a timeout: 0.1 s
+constexpr int kWaitMinPolls = 64;
+
+// Bounded wait for phase `parity` of an mbarrier: true once the phase completes, false
+// when it is still pending after limit_ns of wall-clock time and at least kWaitMinPolls
+// tests (the poll floor keeps a long preemption of the context from counting as a
+// timeout). The caller reports MOE_ERR_TIMEOUT instead of hanging.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    int polls = 1;
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (polls < kWaitMinPolls)
+            polls++;
+        else if (global_ns() - t0 > limit_ns)
+            return false;
     }
-    return false;
 }
 
 // ---------------------------------------------------------------------------

@@ -143,6 +143,7 @@ cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const u
 cudaError_t launch_combine_partitioned(const LaunchCtx& ctx, const uint16_t* partial, int64_t T, int64_t S, int H,
                                        const int32_t* ids, int K, int E, int P, uint16_t* out, int32_t* dev_status);
 
+cudaError_t launch_wait_timeout_check(const LaunchCtx& ctx, int32_t* status, uint64_t limit_ns, int complete);
 cudaError_t launch_fp8_division_check(const LaunchCtx& ctx, unsigned long long* result);
 cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t n, uint8_t* e4m3,
                                  uint8_t* e2m1, float* e4m3_value);

@@ -424,6 +424,22 @@ moe_status_t moe_combine_partitioned(const uint16_t *partial, int64_t num_tokens
 moe_status_t moe_fp8_division_check(unsigned long long *result, moe_stream_t stream);
 
 /*
+ * moe_wait_timeout_check -- diagnostics: runs the bounded wait of the bulk (TMA) dispatch
+ * kernels on one shared-memory mbarrier of arrival count 1, so that its give-up path can be
+ * checked without any fault. With complete = 1 the kernel arrives at the barrier first and
+ * the wait returns at once; with complete = 0 nothing ever arrives, the wait gives up after
+ * limit_ns of wall-clock time and the kernel writes MOE_ERR_TIMEOUT to dev_status (first
+ * error wins) and exits. The dispatch kernels wait the same way with a limit of 1 s per ring
+ * stage (0.1 s for draining their loads after a timeout).
+ * (No counterpart on the pages: a test hook for the library's own bounded waits.)
+ *   dev_status  [1] int32 device status word.
+ *   limit_ns    1 .. 10^10.
+ *   complete    0 or 1.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
+ */
+moe_status_t moe_wait_timeout_check(int32_t *dev_status, int64_t limit_ns, int complete, moe_stream_t stream);
+
+/*
  * moe_convert_probe -- diagnostics: run the number-format conversions of the quantising
  * kernels on arbitrary fp32 inputs, so their rounding, saturation, signed zeros and
  * packing order can be checked against an independent implementation of the formats.

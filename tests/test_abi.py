@@ -170,3 +170,14 @@ def test_division_check_validation(lib):
     f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     assert f(None, None) == 1
     assert f(ctypes.c_void_p(0x1004), None) == 1      # 8-byte alignment
+
+
+def test_wait_timeout_check_validation(lib):
+    f = _c(lib, "moe_wait_timeout_check")
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    st = ctypes.c_void_p(0x1000)
+    assert f(None, 1000, 0, None) == 1                 # no status word
+    assert f(ctypes.c_void_p(0x1002), 1000, 0, None) == 1  # 4-byte alignment
+    assert f(st, 0, 0, None) == 1                      # limit in 1 .. 10^10 ns
+    assert f(st, 10 ** 10 + 1, 0, None) == 1
+    assert f(st, 1000, 2, None) == 1                   # complete is 0 or 1
