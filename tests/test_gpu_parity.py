@@ -88,6 +88,9 @@ def test_qwen3_masked_secondary():
     (1024, 5120, 160, 6, "masked", "fp8g128", 64),
     (200, 2880, 32, 4, "normal", "none", 0),
     (1100, 2880, 32, 4, "masked", "nvfp4b16", 300),
+    # >= 1024 tokens whose rows do not fit the bulk ring's shared memory: the register path
+    (1030, 32768, 16, 2, "normal", "none", 0),
+    (1030, 32768, 16, 2, "masked", "fp8g128", 200),
 ])
 def test_shapes_full(T, H, E, K, mode, quant, M):
     w = make_case(T, H, E, K, seed=T + H + E + K, mode=mode, quant=quant, M=M, invalid_rate=0.05)
