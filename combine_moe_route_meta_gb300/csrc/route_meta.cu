@@ -99,11 +99,15 @@ __device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int 
         if (write) seg_indptr[E] = total;
     }
     __syncthreads();
-    if (write && partition_counts != nullptr && e < P) {
-        const int ep = E / P;
-        int n = 0;
-        for (int x = e * ep; x < (e + 1) * ep; x++) n += hist[x];
-        partition_counts[e] = n;
+    if (write && partition_counts != nullptr) {
+        // warp w sums the histogram over partition w's experts (lane-strided, then reduced)
+        const int ep = E / P, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int p = w; p < P; p += int(blockDim.x >> 5)) {
+            int n = 0;
+            for (int x = p * ep + lane; x < (p + 1) * ep; x += 32) n += hist[x];
+            n = __reduce_add_sync(kFullMask, n);
+            if (lane == 0) partition_counts[p] = n;
+        }
     }
 }
 
@@ -176,18 +180,33 @@ __device__ __forceinline__ void warp_ranks(const int32_t* __restrict__ ids, cons
 // Warp v scans the columns e = v, v+32, ...: lane l holds warp l's count, a 5-step
 // shuffle scan gives every lane its exclusive prefix, lane 31 the column total.
 __device__ __forceinline__ void scan_warps(int* cnt, int* hist, int E) {
+    constexpr int kCols = 4;  // columns scanned together, so their shuffles overlap
     const int lane = threadIdx.x & 31, v = threadIdx.x >> 5;
     const int S = cnt_stride(E);
-    for (int e = v; e < E; e += kWarps) {
-        const int c = cnt[lane * S + e];
-        int x = c;
+    for (int e0 = v; e0 < E; e0 += kWarps * kCols) {
+        int c[kCols], x[kCols];
+#pragma unroll
+        for (int j = 0; j < kCols; j++) {
+            const int e = e0 + j * kWarps;
+            c[j] = e < E ? cnt[lane * S + e] : 0;
+            x[j] = c[j];
+        }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, x, o);
-            if (lane >= o) x += y;
+#pragma unroll
+            for (int j = 0; j < kCols; j++) {
+                const int y = __shfl_up_sync(kFullMask, x[j], o);
+                if (lane >= o) x[j] += y;
+            }
         }
-        cnt[lane * S + e] = x - c;
-        if (lane == 31) hist[e] = x;
+#pragma unroll
+        for (int j = 0; j < kCols; j++) {
+            const int e = e0 + j * kWarps;
+            if (e < E) {
+                cnt[lane * S + e] = x[j] - c[j];
+                if (lane == 31) hist[e] = x[j];
+            }
+        }
     }
 }
 
