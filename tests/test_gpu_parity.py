@@ -91,6 +91,10 @@ def test_qwen3_masked_secondary():
     # >= 1024 tokens whose rows do not fit the bulk ring's shared memory: the register path
     (1030, 32768, 16, 2, "normal", "none", 0),
     (1030, 32768, 16, 2, "masked", "fp8g128", 200),
+    # many short rows: each bulk CTA cycles its ring (and its mbarrier phases) 100+ times
+    (200000, 128, 16, 2, "normal", "none", 0),
+    (100000, 512, 16, 2, "masked", "fp8g128", 15000),
+    (100000, 256, 16, 2, "normal", "nvfp4b16", 0),
 ])
 def test_shapes_full(T, H, E, K, mode, quant, M):
     w = make_case(T, H, E, K, seed=T + H + E + K, mode=mode, quant=quant, M=M, invalid_rate=0.05)
