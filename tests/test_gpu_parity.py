@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import bf16_bits_to_f32, f32_to_bf16_bits, make_case, make_workload
+from workloads import bf16_bits_to_f32, f32_to_bf16_bits, make_case, make_workload, random_bf16
 
 from _harness import (bytes_of, check_combine, gpu_meta, moe, run_full, run_sampled, to_dev)
 
@@ -232,7 +232,7 @@ def test_repeated_calls_reuse_workspace():
 @pytest.mark.parametrize("case", ["decode", "normal_4096"])
 def test_dispatcher_graph_capture_replays_correctly(case):
     """route + dispatch + combine captured in one CUDA graph and replayed (decode: one-block
-    metadata; normal_4096: the cooperative multi-block metadata and the bulk dispatch)."""
+    metadata; normal_4096: the count and place metadata kernels and the bulk dispatch)."""
     m = moe()
     if case == "decode":
         w = make_workload("decode")
@@ -267,6 +267,61 @@ def test_dispatcher_graph_capture_replays_correctly(case):
     assert torch.equal(d.out_q, ref_q)
     assert torch.equal(d.out, ref_out)
     d.check()
+
+
+def test_concurrent_streams_keep_their_own_results():
+    """Four dispatchers on four streams, their launches interleaved with no ordering between
+    the streams (fused small batch, count + place metadata with the bulk FP8 dispatch,
+    NVFP4 masked, bf16 register path): every call works only on its caller's buffers, so
+    each stream's results match the oracle."""
+    import oracle as orc
+    m = moe()
+    cases = [make_case(96, 1024, 32, 4, seed=61, mode="masked", quant="fp8g128", M=48, invalid_rate=0.05),
+             make_case(3000, 1024, 64, 8, seed=62, quant="fp8g128", routing="zipf"),
+             make_case(1500, 512, 16, 4, seed=63, mode="masked", quant="nvfp4b16", M=600),
+             make_case(700, 768, 24, 3, seed=64)]
+    streams = [torch.cuda.Stream() for _ in cases]
+    runs = []
+    for w, s in zip(cases, streams):
+        x, ids, wt = to_dev(w)
+        d = m.MoEDispatcher(w.T, w.H, w.K, w.E, mode=w.mode, quant=w.quant, num_partitions=w.P,
+                            max_tokens_per_expert=w.M)
+        eo_rows = w.E * w.M if w.mode == "masked" else w.T * w.K
+        eo_h = random_bf16(np.random.default_rng(w.seed), (eo_rows, w.H))
+        eo = torch.from_numpy(eo_h.view(np.int16)).cuda().view(torch.bfloat16)
+        runs.append((w, s, d, x, ids, wt, eo, eo_h))
+    torch.cuda.synchronize()
+    for step in range(3):  # interleave the streams' launches call by call
+        for w, s, d, x, ids, wt, eo, _ in runs:
+            with torch.cuda.stream(s):
+                if step == 0:
+                    d.route(ids)
+                elif step == 1:
+                    d.dispatch(x, ids, w.global_scale or 0.0)
+                else:
+                    d.combine(eo, ids, wt)
+    torch.cuda.synchronize()
+    for w, s, d, x, ids, wt, eo, eo_h in runs:
+        d.check()
+        om = orc.route_meta(w.topk_ids, w.E, P=w.P, M=w.M)
+        assert np.array_equal(d.src2dst.cpu().numpy(), om.src2dst)
+        oq, osc = orc.dispatch(w.mode, w.quant, w.x, w.topk_ids, om, w.E, M=w.M,
+                               global_scale=w.global_scale or 0.0)
+        pairs = [(bytes_of(d.out_q), np.ascontiguousarray(oq).view(np.uint8))]
+        if osc is not None:
+            pairs.append((bytes_of(d.out_scales), np.ascontiguousarray(osc).view(np.uint8)))
+        for got, ref in pairs:
+            if w.mode == "masked":
+                got, ref = got.reshape(w.E, w.M, -1), ref.reshape(w.E, w.M, -1)
+                for e in range(w.E):
+                    n = int(om.masked_m[e])
+                    assert np.array_equal(got[e, :n], ref[e, :n])
+            else:
+                n = om.num_valid
+                got, ref = got.reshape(w.T * w.K, -1), ref.reshape(w.T * w.K, -1)
+                assert np.array_equal(got[:n], ref[:n])
+        want = orc.combine(w.mode, eo_h, w.topk_ids, w.topk_weights, om, w.E, M=w.M)
+        check_combine(d.out.view(torch.int16).cpu().numpy().view(np.uint16), want)
 
 
 # --- moe_route_dispatch: route + dispatch in one call -------------------------------------
