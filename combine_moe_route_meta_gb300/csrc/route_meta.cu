@@ -72,10 +72,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
 // hist[e] (e < E) -> seg (shared, E+1 ints), seg_indptr, masked_m, partition_counts.
 // Segments are padded to a multiple of A rows (expert_alignment; A = 1: no padding).
 // With `write` false only the shared seg[] is produced; with `write` the per-expert outputs
-// go to memory, including -1 in reorder_topk_ids for every padding row.
+// go to memory (the padding rows of reorder_topk_ids: write_padding).
 __device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int E, int P, int M, int A,
                                  int64_t* seg_indptr, int32_t* masked_m, int32_t* partition_counts,
-                                 int32_t* reorder, int32_t* status, bool write = true) {
+                                 int32_t* status, bool write = true) {
     const int e = threadIdx.x;  // E <= 1024 == blockDim
     const int c = e < E ? hist[e] : 0;
     const int padded = (c + A - 1) / A * A;
@@ -91,7 +91,6 @@ __device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int 
                 set_status(status, MOE_ERR_CAPACITY);
             }
             masked_m[e] = mm;
-            for (int r = c; r < padded; r++) reorder[excl + r] = -1;
         }
     }
     if (e == 0) {
@@ -108,6 +107,20 @@ __device__ void finish_histogram(const int* hist, int* seg, int* warp_sums, int 
             n = __reduce_add_sync(kFullMask, n);
             if (lane == 0) partition_counts[p] = n;
         }
+    }
+}
+
+// -1 in reorder_topk_ids on the padding rows [seg[e] + hist[e], seg[e] + roundup(hist[e], A)) of
+// every expert's segment (A > 1 only). One warp per expert, its lanes on consecutive rows;
+// the experts are dealt out over `parts` blocks, this block taking share `part`. Needs the
+// final seg[] (shared, as left by finish_histogram).
+__device__ void write_padding(const int* hist, const int* seg, int E, int A, int32_t* reorder, int part, int parts) {
+    if (A == 1) return;
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = int(blockDim.x >> 5);
+    for (int e = part * nw + w; e < E; e += parts * nw) {
+        const int c = hist[e];
+        const int padded = (c + A - 1) / A * A;
+        for (int r = c + lane; r < padded; r += 32) reorder[seg[e] + r] = -1;
     }
 }
 
@@ -253,7 +266,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_meta_single_kernel(Rou
     scan_warps(cnt, hist, E);
     __syncthreads();
     finish_histogram(hist, seg, warp_sums, E, a.P, a.M, a.A, a.seg_indptr, a.masked_m,
-                     a.partition_counts, a.reorder, a.status);
+                     a.partition_counts, a.status);
+    write_padding(hist, seg, E, a.A, a.reorder, 0, 1);
     // finish_histogram ends with __syncthreads: seg[] and the warp offsets in cnt are final
 #pragma unroll
     for (int r = 0; r < RMAX; r++) {
@@ -374,7 +388,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_meta_place_kernel(RouteAr
 
     table_column_sums(a.table, B, b, E, part_pre, part_tot, pre, tot);
     finish_histogram(tot, seg, warp_sums, E, a.P, a.M, a.A, a.seg_indptr, a.masked_m, a.partition_counts,
-                     a.reorder, a.status, b == 0);
+                     a.status, b == 0);
+    write_padding(tot, seg, E, a.A, a.reorder, b, B);
 
     for (int64_t i = i0 + tid; i < i1; i += blockDim.x) {
         const bool first = i == i0 + tid;
