@@ -57,6 +57,15 @@ struct DispatchArgs {
     int64_t n_units;
     int64_t max_row;  // exclusive bound on normal-mode rows (the output's row capacity)
     ScaleLayout L;
+    // one-row-per-partition destinations (FlashInfer layout, bulk kernels with PART): row
+    // p*S + t for every partition p < P owning one of token t's experts, plus the receive ids
+    // (sanitised to invalid_id) and weights of every partition's row of the token
+    int P, ep;
+    int64_t S;
+    int32_t invalid_id;
+    const float* w;
+    int32_t* recv_ids;
+    float* recv_w;
 };
 
 // destination row of pair t*K + lane (lanes >= K return -1); s_seg: seg_indptr in smem
@@ -126,6 +135,72 @@ __global__ void __launch_bounds__(kDispatchThreads) dispatch_kernel(DispatchArgs
 // Whole-row bulk stores keep each destination's bytes together in DRAM (a probe of this
 // pattern ran at 5.8 TB/s against 5.0 TB/s for 512-byte warp slices).
 // ---------------------------------------------------------------------------
+// Warp-collective (all 32 lanes): lane p's destination row for token t in the partition
+// layout, p*S + t when partition p (< P) owns one of the token's experts, else -1. my_id /
+// my_w: the token's id and weight of slot `lane` (lanes >= K: -1 / 0), loaded by the caller.
+// The same warp writes the token's receive ids (ids the partition does not own ->
+// invalid_id) and weights (routed partitions only) for every partition.
+__device__ __forceinline__ int64_t partition_row(const DispatchArgs& a, int64_t t, int lane, int my_id,
+                                                 float my_w) {
+    const bool valid = my_id >= 0 && my_id < a.E;
+    if (!valid && my_id != -1 && lane < a.K) set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
+    bool routed = false;
+    for (int k = 0; k < a.K; k++) {
+        const int e = __shfl_sync(kFullMask, my_id, k);
+        routed |= e >= 0 && e < a.E && e / a.ep == lane;
+    }
+    routed = routed && lane < a.P;
+    for (int p = 0; p < a.P; p++) {
+        const bool rp = __shfl_sync(kFullMask, routed, p);
+        if (lane < a.K) {
+            const int64_t r = (int64_t(p) * a.S + t) * a.K + lane;
+            a.recv_ids[r] = (rp && valid && my_id / a.ep == p) ? my_id : a.invalid_id;
+            if (rp) a.recv_w[r] = my_w;
+        }
+    }
+    return routed ? int64_t(lane) * a.S + t : -1;
+}
+
+// Token metadata of the partition layout, loaded one token ahead by the warp that resolves
+// the destination rows: the ids and weights are inputs that no earlier kernel of the call
+// has brought into L2, so each token would otherwise wait a DRAM round trip for them.
+struct PartMeta {
+    int id = -1;
+    float w = 0.0f;
+    __device__ __forceinline__ void load(const DispatchArgs& a, int64_t t, int lane) {
+        if (lane < a.K) {
+            id = __ldg(a.ids + t * a.K + lane);
+            w = __ldg(a.w + t * a.K + lane);
+        }
+    }
+};
+
+// Warp-collective destination row of lane `lane` for token t in the bulk kernels: pair
+// t*K + lane of the expert layouts, or partition `lane` of the partition layout (PART; `pm`
+// holds token t's metadata on entry and the next token's, tn < T, on return).
+template <bool MASKED, bool PART>
+__device__ __forceinline__ int64_t bulk_dest_row(const DispatchArgs& a, const int* s_seg, int64_t t, int lane,
+                                                 PartMeta& pm, int64_t tn) {
+    if constexpr (PART) {
+        const PartMeta cur = pm;
+        if (tn < a.T) pm.load(a, tn, lane);
+        return partition_row(a, t, lane, cur.id, cur.w);
+    } else {
+        return dest_row<MASKED>(a, s_seg, t, lane);
+    }
+}
+
+// Partition layout: the receive ids of the padding slots t in [T, S) of every partition are
+// invalid_id (grid-stride over all threads of the grid).
+__device__ __forceinline__ void partition_padding_ids(const DispatchArgs& a) {
+    const int64_t per_p = (a.S - a.T) * a.K;
+    const int64_t pad = per_p * a.P;
+    for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < pad; j += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t p = j / per_p, rem = j - p * per_p;
+        a.recv_ids[(p * a.S + a.T) * a.K + rem] = a.invalid_id;
+    }
+}
+
 struct BulkGeom {
     uint32_t in_bytes;   // 2H: one bf16 row
     uint32_t q_bytes;    // quantised row (2H for the copy)
@@ -137,7 +212,8 @@ struct BulkGeom {
 
 constexpr int kBulkCopyThreads = 32;
 constexpr int kBulkQuantThreads = 256;
-constexpr uint32_t kBulkHeader = 512;  // mbarriers (8 B each) and destination rows (2 x 16 x 8 B)
+constexpr uint32_t kBulkHeader = 768;  // mbarriers (8 B each) at 0, destination rows (2 x 32 x 8 B) at 256
+constexpr int kBulkRows = 32;          // destination rows per token: K <= 16 pairs, or P <= 32 partitions
 
 template <bool MASKED>
 __device__ __forceinline__ void stage_seg(const DispatchArgs& a, int* s_seg) {
@@ -145,11 +221,13 @@ __device__ __forceinline__ void stage_seg(const DispatchArgs& a, int* s_seg) {
         stage_to_shared(a.seg, s_seg, a.E);
 }
 
-// copy mode: lane 0 drives the ring, lanes < K resolve the destination rows
-template <bool MASKED>
+// copy mode: lane 0 drives the ring, lanes < K (partitions < P) resolve the destination rows
+template <bool MASKED, bool PART>
 __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(DispatchArgs a, BulkGeom geo) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait();
+    if constexpr (PART) partition_padding_ids(a);
+    const int nd = PART ? a.P : a.K;
     const int lane = threadIdx.x & 31, NS = geo.stages;
     const uint32_t bar0 = smem_addr(smem), in0 = smem_addr(smem + geo.in_off);
     int* s_seg = reinterpret_cast<int*>(smem + geo.out_off);
@@ -161,6 +239,8 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
     __syncwarp();
     const int64_t G = gridDim.x;
     const int64_t ntok = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / G + 1 : 0;
+    PartMeta pm;  // PART: the first token's ids and weights (warp 0), then one token ahead
+    if (PART && threadIdx.x < 32 && ntok > 0) pm.load(a, blockIdx.x, threadIdx.x & 31);
     int64_t issued = 0, consumed = 0;  // lane 0's counts of loads issued / completed
     auto issue = [&](int64_t i) {
         const int s = int(i % NS);
@@ -172,7 +252,7 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
     for (int64_t i = 0; i < ntok; i++) {
         const int64_t t = blockIdx.x + i * G;
         const int s = int(i % NS);
-        const int64_t my_row = dest_row<MASKED>(a, s_seg, t, lane);
+        const int64_t my_row = bulk_dest_row<MASKED, PART>(a, s_seg, t, lane, pm, t + G);
         int ok = 1;
         if (lane == 0) {
             if (i + NS - 1 < ntok) {
@@ -187,7 +267,7 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
             if (lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
             break;
         }
-        for (int k = 0; k < a.K; k++) {
+        for (int k = 0; k < nd; k++) {
             const int64_t row = __shfl_sync(kFullMask, my_row, k);
             if (lane == 0 && row >= 0)
                 bulk_store(static_cast<uint8_t*>(a.out_q) + row * geo.q_bytes, in0 + s * geo.in_bytes, geo.q_bytes);
@@ -202,14 +282,15 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
 }
 
 // quantising modes: 256 threads quantise shared -> shared; thread 0 drives the copies
-template <int QUANT, bool MASKED>
+template <int QUANT, bool MASKED, bool PART, bool SWZ>
 __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(DispatchArgs a, BulkGeom geo) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait();
+    if constexpr (PART) partition_padding_ids(a);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthreads = blockDim.x;
-    const int NS = geo.stages, H = a.H;
+    const int NS = geo.stages, H = a.H, nd = PART ? a.P : a.K;
     const uint32_t bar0 = smem_addr(smem);
-    int64_t* s_rows = reinterpret_cast<int64_t*>(smem + 256);  // [2][16]
+    int64_t* s_rows = reinterpret_cast<int64_t*>(smem + 256);  // [2][kBulkRows]
     unsigned char* in_base = smem + geo.in_off;
     unsigned char* out_base = smem + geo.out_off;                // [2][q_bytes + s_bytes]
     int* s_seg = reinterpret_cast<int*>(out_base + 2 * (geo.q_bytes + geo.s_bytes));
@@ -223,6 +304,8 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
     __syncthreads();
     const int64_t G = gridDim.x;
     const int64_t ntok = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / G + 1 : 0;
+    PartMeta pm;  // PART: the first token's ids and weights (warp 0), then one token ahead
+    if (PART && threadIdx.x < 32 && ntok > 0) pm.load(a, blockIdx.x, threadIdx.x & 31);
     int64_t issued = 0, consumed = 0;  // thread 0's counts of loads issued / completed
     auto issue = [&](int64_t i) {
         const int s = int(i % NS);
@@ -236,8 +319,8 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
         const int64_t t = blockIdx.x + i * G;
         const int s = int(i % NS), o = int(i & 1);
         if (warp == 0) {
-            const int64_t r = dest_row<MASKED>(a, s_seg, t, lane);
-            if (lane < a.K) s_rows[o * 16 + lane] = r;
+            const int64_t r = bulk_dest_row<MASKED, PART>(a, s_seg, t, lane, pm, t + G);
+            if (lane < nd) s_rows[o * kBulkRows + lane] = r;
         }
         if (tid == 0) {
             if (i + NS - 1 < ntok) issue(i + NS - 1);  // its stage was last read before the previous barrier
@@ -278,15 +361,31 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
         }
         fence_proxy_async();
         __syncthreads();
+        // SWZ (NVFP4 only): scales in the 128 x 4 tile layout, stored by the threads below
+        constexpr bool swizzled = SWZ && QUANT == MOE_QUANT_NVFP4_B16;
         if (tid == 0) {
-            for (int k = 0; k < a.K; k++) {
-                const int64_t row = s_rows[o * 16 + k];
+            for (int k = 0; k < nd; k++) {
+                const int64_t row = s_rows[o * kBulkRows + k];
                 if (row < 0) continue;
                 bulk_store(static_cast<uint8_t*>(a.out_q) + row * geo.q_bytes, out0 + o * out_bytes, geo.q_bytes);
-                bulk_store(static_cast<uint8_t*>(a.out_s) + row * geo.s_bytes, out0 + o * out_bytes + geo.q_bytes,
-                           geo.s_bytes);
+                if (!swizzled)
+                    bulk_store(static_cast<uint8_t*>(a.out_s) + row * geo.s_bytes, out0 + o * out_bytes + geo.q_bytes,
+                               geo.s_bytes);
             }
             bulk_commit();
+        }
+        if constexpr (swizzled) {
+            // block scales in the 128 x 4 tile layout: 4 consecutive columns of a row are 4
+            // contiguous bytes, so every destination row takes C/4 word stores from the staged row
+            const int C4 = H / 64;
+            for (int j = tid; j < nd * C4; j += nthreads) {
+                const int k = j / C4, c4 = j - k * C4;
+                const int64_t row = s_rows[o * kBulkRows + k];
+                if (row >= 0)
+                    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out_s) +
+                                                 swizzled_128x4_index(row, 4 * c4, H / 16)) =
+                        *reinterpret_cast<const uint32_t*>(so + 4 * c4);
+            }
         }
     }
     if (tid == 0) {
@@ -308,9 +407,12 @@ BulkGeom bulk_geometry(int quant, const DispatchArgs& a) {
         case MOE_QUANT_FP8_G128_UE8M0: g.q_bytes = uint32_t(H); g.s_bytes = uint32_t(H / 128); break;
         default: g.q_bytes = uint32_t(H / 2); g.s_bytes = uint32_t(H / 16); break;
     }
+    // swizzled NVFP4 scales are written in 4-byte pieces by the threads (not as a bulk row),
+    // so only the row-major scale array needs a 16-byte aligned base
+    const bool swizzled = a.L.kind == MOE_SCALES_SWIZZLED_128X4 && quant == MOE_QUANT_NVFP4_B16;
     const bool aligned16 = (reinterpret_cast<uintptr_t>(a.out_s) & 15) == 0;
-    if (g.q_bytes % 16 || g.s_bytes % 16 || a.L.kind != MOE_SCALES_ROW_MAJOR ||
-        (quant != MOE_QUANT_NONE && !aligned16))
+    if (g.q_bytes % 16 || g.s_bytes % 16 || (a.L.kind != MOE_SCALES_ROW_MAJOR && !swizzled) ||
+        (quant != MOE_QUANT_NONE && !swizzled && !aligned16))
         return g;
     const uint32_t seg_bytes = uint32_t(sizeof(int)) * uint32_t(a.E);
     // ring depth, measured on GB300 (prefill / qwen3 / nvfp4 shapes): the copy mode is flat
@@ -329,14 +431,14 @@ size_t bulk_smem(int quant, const BulkGeom& g, int E) {
     return size_t(g.out_off) + (quant == MOE_QUANT_NONE ? 0 : 2 * (g.q_bytes + g.s_bytes)) + sizeof(int) * size_t(E);
 }
 
-template <int QUANT, bool MASKED>
+template <int QUANT, bool MASKED, bool PART = false>
 cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkGeom& geo) {
     const size_t smem = bulk_smem(QUANT, geo, a.E);
     int threads;
     int per_sm = 0;
     cudaError_t err;
     if constexpr (QUANT == MOE_QUANT_NONE) {
-        auto kern = dispatch_bulk_copy_kernel<MASKED>;
+        auto kern = dispatch_bulk_copy_kernel<MASKED, PART>;
         threads = kBulkCopyThreads;
         err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (err == cudaSuccess) err = blocks_per_sm(ctx, kern, threads, smem, &per_sm);
@@ -344,7 +446,9 @@ cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkG
         const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1)));
         return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
     } else {
-        auto kern = dispatch_bulk_quant_kernel<QUANT, MASKED>;
+        auto kern = dispatch_bulk_quant_kernel<QUANT, MASKED, PART, false>;
+        if constexpr (QUANT == MOE_QUANT_NVFP4_B16)
+            if (a.L.kind == MOE_SCALES_SWIZZLED_128X4) kern = dispatch_bulk_quant_kernel<QUANT, MASKED, PART, true>;
         // as many passes over the row's 16-element slices as 256 threads need, with the block
         // sized so that every pass is full (H = 7168: 448 slices = 2 x 224, not 256 + 192)
         const int nslices = a.H / kLaneElems;
@@ -484,6 +588,42 @@ cudaError_t launch_sf_swizzle_pad(const LaunchCtx& ctx, uint8_t* sf, int64_t R, 
     const int threads = 256;
     return launch_pdl(ctx, sf_swizzle_pad_kernel, dim3(unsigned((n_words + threads - 1) / threads)), dim3(threads),
                       0, sf, R, C, n_words);
+}
+
+cudaError_t launch_dispatch_partitioned_bulk(const LaunchCtx& ctx, int quant, const uint16_t* x, int64_t T,
+                                             int64_t S, int H, const int32_t* ids, const float* w, int K, int E,
+                                             int P, int32_t invalid_id, float g, void* recv_x, uint8_t* recv_sf,
+                                             int32_t* recv_ids, float* recv_w, int32_t* dev_status,
+                                             int scale_layout, bool* launched) {
+    *launched = false;
+    if (T < kBulkMinTokens || (quant != MOE_QUANT_NONE && quant != MOE_QUANT_NVFP4_B16)) return cudaSuccess;
+    DispatchArgs a{};
+    a.x = x;
+    a.T = T;
+    a.H = H;
+    a.K = K;
+    a.E = E;
+    a.ids = ids;
+    a.g = g;
+    a.out_q = recv_x;
+    a.out_s = recv_sf;
+    a.status = dev_status;
+    a.units_per_row = (H + kSlice - 1) / kSlice;
+    a.n_units = T * a.units_per_row;
+    a.max_row = int64_t(P) * S;
+    a.L = ScaleLayout{scale_layout, 0, 0};
+    a.P = P;
+    a.ep = E / P;
+    a.S = S;
+    a.invalid_id = invalid_id;
+    a.w = w;
+    a.recv_ids = recv_ids;
+    a.recv_w = recv_w;
+    const BulkGeom geo = bulk_geometry(quant, a);
+    if (geo.stages == 0) return cudaSuccess;
+    *launched = true;
+    return quant == MOE_QUANT_NVFP4_B16 ? launch_bulk<MOE_QUANT_NVFP4_B16, false, true>(ctx, a, geo)
+                                        : launch_bulk<MOE_QUANT_NONE, false, true>(ctx, a, geo);
 }
 
 cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uint16_t* x, int64_t T,

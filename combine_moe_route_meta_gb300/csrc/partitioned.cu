@@ -76,6 +76,53 @@ __global__ void __launch_bounds__(kThreads) dispatch_layout_kernel(const int32_t
             if (s_exp[e]) atomicAdd(nte + e, s_exp[e]);
 }
 
+// One block for batches whose T*K ids fit in shared memory (<= kLayoutSingleMaxPairs): the
+// ids are staged in one round of loads, the counters live in shared memory and are written
+// out whole at the end, so there is no global atomic and no clearing of the outputs first.
+constexpr int kLayoutSingleThreads = 1024;
+__global__ void __launch_bounds__(kLayoutSingleThreads)
+    dispatch_layout_single_kernel(const int32_t* __restrict__ ids, int T, int K, int E, int P, int32_t* ntr,
+                                  uint8_t* itr, int32_t* nte, int32_t* status) {
+    extern __shared__ int s_lay[];  // [P] tokens per partition | [E] pairs per expert | [T*K] ids
+    int* s_rank = s_lay;
+    int* s_exp = s_rank + P;
+    int* s_ids = s_exp + E;
+    for (int j = threadIdx.x; j < P + E; j += blockDim.x) s_lay[j] = 0;
+    pdl_wait();
+    stage_to_shared(ids, s_ids, T * K);
+    __syncthreads();
+    const int ep = E / P;
+    bool bad = false;
+    for (int t = threadIdx.x; t < T; t += blockDim.x) {
+        const int* tid_ids = s_ids + t * K;
+        uint8_t* row = itr + int64_t(t) * P;
+        for (int p = 0; p < P; p++) row[p] = 0;
+        for (int k = 0; k < K; k++) {
+            const int e = tid_ids[k];
+            if (e < 0 || e >= E) {
+                bad |= e != -1;
+                continue;
+            }
+            atomicAdd(&s_exp[e], 1);
+            const int p = e / ep;
+            bool seen = false;  // an earlier slot of this token in the same partition
+            for (int k2 = 0; k2 < k; k2++) {
+                const int e2 = tid_ids[k2];
+                seen |= e2 >= 0 && e2 < E && e2 / ep == p;
+            }
+            if (!seen) {
+                row[p] = 1;
+                atomicAdd(&s_rank[p], 1);
+            }
+        }
+    }
+    if (__any_sync(kFullMask, bad) && (threadIdx.x & 31) == 0) set_status(status, MOE_ERR_BAD_EXPERT_ID);
+    __syncthreads();
+    for (int p = threadIdx.x; p < P; p += blockDim.x) ntr[p] = s_rank[p];
+    if (nte != nullptr)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) nte[e] = s_exp[e];
+}
+
 struct PartArgs {
     const uint16_t* x;
     const int32_t* ids;
@@ -227,6 +274,16 @@ cudaError_t launch_units(const LaunchCtx& ctx, Kernel kern, const PartArgs& a, i
 cudaError_t launch_dispatch_layout(const LaunchCtx& ctx, const int32_t* ids, int64_t T, int K, int E, int P,
                                    int32_t* num_tokens_per_rank, uint8_t* is_token_in_rank,
                                    int32_t* num_tokens_per_expert, int32_t* dev_status) {
+    if (T * K <= kLayoutSingleMaxPairs) {
+        const size_t smem = sizeof(int) * size_t(P + E + T * K);
+        if (smem > 48 * 1024) {
+            cudaError_t err = cudaFuncSetAttribute(dispatch_layout_single_kernel,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            if (err != cudaSuccess) return err;
+        }
+        return launch_pdl(ctx, dispatch_layout_single_kernel, dim3(1), dim3(kLayoutSingleThreads), smem, ids,
+                          int(T), K, E, P, num_tokens_per_rank, is_token_in_rank, num_tokens_per_expert, dev_status);
+    }
     cudaError_t err = cudaMemsetAsync(num_tokens_per_rank, 0, sizeof(int32_t) * size_t(P), ctx.stream);
     if (err == cudaSuccess && num_tokens_per_expert)
         err = cudaMemsetAsync(num_tokens_per_expert, 0, sizeof(int32_t) * size_t(E), ctx.stream);
@@ -266,6 +323,11 @@ cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const u
         cudaError_t err = launch_sf_swizzle_pad(ctx, recv_sf, int64_t(P) * S, H / 16);
         if (err != cudaSuccess) return err;
     }
+    bool bulk = false;
+    cudaError_t err = launch_dispatch_partitioned_bulk(ctx, quant, x, T, S, H, ids, w, K, E, P, invalid_id, g,
+                                                       recv_x, recv_sf, recv_ids, recv_w, dev_status, scale_layout,
+                                                       &bulk);
+    if (err != cudaSuccess || bulk) return err;
     const int64_t pad = (S - T) * P * K;
     if (a.n_units == 0 && pad == 0) return cudaSuccess;
     if (quant == MOE_QUANT_NVFP4_B16) return launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NVFP4_B16>, a, pad);

@@ -340,7 +340,9 @@ moe_status_t moe_combine(moe_mode_t mode, const uint16_t *expert_out, int64_t nu
  * Arguments: topk_ids [T, K] int32; num_partitions (P) >= 1 with E % P == 0;
  * num_tokens_per_rank [P] int32 out; is_token_in_rank [T, P] uint8 out (0/1);
  * num_tokens_per_expert [E] int32 out or NULL. Ids outside [-1, E) are skipped and reported
- * as MOE_ERR_BAD_EXPERT_ID in *dev_status. The counts are cleared on `stream` first.
+ * as MOE_ERR_BAD_EXPERT_ID in *dev_status. Every output is written in full (the caller need not
+ * clear them): up to 4096 (token, k) pairs by one block that writes the counts at the end,
+ * above that by clearing the counts on `stream` and accumulating them with atomics.
  * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
  */
 moe_status_t moe_dispatch_layout(const int32_t *topk_ids, int64_t num_tokens, int topk, int num_experts,

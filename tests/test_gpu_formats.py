@@ -259,9 +259,12 @@ def test_ue8m0_bulk_path_normal_layout():
 
 @pytest.mark.parametrize("mode,T,H,E,K,M", [
     ("normal", 300, 1024, 24, 6, 0),     # 1800 rows -> padded to 1920
-    ("normal", 1500, 2048, 64, 8, 0),    # a batch the row-major NVFP4 path sends to the bulk kernel
+    ("normal", 1500, 2048, 64, 8, 0),    # >= 1024 tokens: the bulk kernel, its threads storing the scales
+    ("normal", 1030, 256, 16, 3, 0),     # bulk kernel, 3090 rows -> padded to 3200
     ("masked", 96, 1024, 16, 4, 30),     # E*M = 480 rows -> padded to 512
     ("masked", 128, 7168, 256, 8, 128),  # the decode shape: 32768 rows, no padding
+    ("masked", 1100, 7168, 64, 8, 200),  # bulk kernel, masked rows
+    ("masked", 1100, 1088, 64, 8, 200),  # H % 256 != 0: swizzled scales from the register path
 ])
 def test_nvfp4_swizzled_scales_match_oracle_interleave(mode, T, H, E, K, M):
     """The whole scale buffer equals the oracle's row-major scales (untouched rows keep

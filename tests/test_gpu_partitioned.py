@@ -19,6 +19,9 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("T,E,K,P,bad", [
     (0, 16, 4, 4, 0.0), (1, 8, 2, 1, 0.0), (300, 64, 6, 8, 0.0), (5000, 256, 8, 32, 0.02), (16384, 128, 8, 8, 0.0),
+    (500, 256, 8, 8, 0.02),        # one block, bad ids reported
+    (512, 1024, 8, 1024, 0.0),     # the largest one-block case: 4096 ids and 2 x 1024 counters in shared memory
+    (513, 1024, 8, 1024, 0.0),     # one token more: the multi-block kernel
 ])
 def test_dispatch_layout_matches_oracle(T, E, K, P, bad):
     m = moe()
@@ -45,6 +48,11 @@ def test_dispatch_layout_matches_oracle(T, E, K, P, bad):
     (512, 600, 4096, 128, 8, 8, "none", 128),
     (37, 37, 128, 64, 16, 32, "none", -1),          # P = 32 (one lane per partition), K = 16
     (20, 20, 64, 4, 2, 1, "nvfp4b16", -1),          # a single partition
+    # >= 1024 tokens with 16-byte row geometry: the bulk (TMA) kernels
+    (1100, 1200, 2048, 64, 8, 8, "nvfp4b16", -1),   # padding slots
+    (1030, 1030, 512, 32, 4, 4, "none", 32),        # invalid id = E
+    (2000, 2050, 256, 64, 16, 32, "nvfp4b16", -1),  # K = 16, P = 32
+    (1024, 1024, 1088, 16, 2, 2, "nvfp4b16", -1),   # H % 256 != 0: NVFP4 stays on the register path
 ])
 def test_partitioned_dispatch_and_combine_match_oracle(T, S, H, E, K, P, quant, inv):
     m = moe()
@@ -115,6 +123,8 @@ def test_partitioned_nvfp4_workload_layout_and_sampled_rows():
     (20, 20, 64, 4, 2, 1),            # 20 rows -> padded to 128
     (50, 61, 1024, 32, 6, 8),         # 488 rows -> padded to 512, padding slots
     (128, 128, 7168, 256, 8, 8),      # the FlashInfer NVFP4 payload shape, 1024 rows
+    (1100, 1130, 2048, 64, 8, 8),     # >= 1024 tokens: the bulk kernel, padding slots
+    (1030, 1030, 256, 96, 6, 32),     # bulk kernel, 32 partitions, 32960 rows -> padded to 33024
 ])
 def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
     """moe_dispatch_partitioned_ex with swizzled scales equals the row-major receive scales
