@@ -759,6 +759,166 @@ def run_gpu(args, w, rank, world, dist):
     return line
 
 
+# ---------------------------------------------------------------------------
+# the NEXT rows (FlashInfer layout, dispatch layout, DeepGEMM formats, int64 ids, FP8
+# pass-through): one timed call each, inputs in HBM, L2 flushed before every call
+# ---------------------------------------------------------------------------
+
+def run_next_rows(args):
+    """One JSON line per NEXT-row call: median CUDA-event time of K calls after an L2 flush,
+    the call's algorithmic bytes, GB/s and fraction of the measured copy bandwidth."""
+    import torch
+    import combine_moe_route_meta_gb300 as moe
+    from workloads import make_workload
+
+    dev = torch.device("cuda", 0)
+    peak, peak_src = measured_hbm_gbs()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_out = torch.empty((), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed_us(fn):
+        for _ in range(args.warmup):
+            fn()
+        ev = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            torch.amax(flush_rd, dim=0, out=flush_out)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(x.elapsed_time(y) for x, y in ev) * 1e3
+
+    def emit(row, call, workload, T, us, nbytes, kernels, launches):
+        gbs = nbytes / us / 1e3
+        print(json.dumps({"row": row, "call": call, "workload": workload, "T": T, "us": us,
+                          "tokens_per_s": T / us * 1e6, "algorithmic_bytes": nbytes, "gbs": gbs,
+                          "peak": peak, "peak_source": peak_src, "frac": gbs / peak,
+                          "kernels": kernels, "launches_per_call": launches,
+                          "steps": args.steps, "warmup": args.warmup,
+                          "l2": "flushed before every call"}), flush=True)
+
+    def dev_in(w):
+        x = torch.from_numpy(w.x.view(np.int16)).to(dev).view(torch.bfloat16)
+        return x, torch.from_numpy(w.topk_ids).to(dev), torch.from_numpy(w.topk_weights).to(dev)
+
+    st = moe.new_status(dev)
+
+    # f1: FlashInfer one-row-per-partition layout (the NVFP4 workload's tokens, 8 partitions,
+    # one receive slot per token)
+    w = make_workload("nvfp4", seed=0)
+    x, ids, wt = dev_in(w)
+    T, H, K, E, P = w.T, w.H, w.K, w.E, w.P
+    S = T
+    ep = E // P
+    flat = w.topk_ids
+    parts = np.zeros((T, P), bool)
+    for k in range(K):
+        e = flat[:, k]
+        ok = (e >= 0) & (e < E)
+        parts[np.nonzero(ok)[0], e[ok] // ep] = True
+    routed = int(parts.sum())
+    g = w.global_scale
+    for quant, layout in (("nvfp4b16", "row"), ("nvfp4b16", "swizzled"), ("none", "row")):
+        rx = torch.empty((P, S, H // 2 if quant == "nvfp4b16" else H),
+                         dtype=torch.uint8 if quant == "nvfp4b16" else torch.bfloat16, device=dev)
+        rsf = None
+        if quant == "nvfp4b16":
+            rsf = torch.empty((moe.swizzled_scale_bytes(P * S, H),) if layout == "swizzled" else (P, S, H // 16),
+                              dtype=torch.uint8, device=dev)
+        rids = torch.empty((P, S, K), dtype=torch.int32, device=dev)
+        rw = torch.empty((P, S, K), dtype=torch.float32, device=dev)
+        rb = row_bytes(quant, H)
+        nbytes = 2 * T * H + 8 * T * K + P * S * 4 * K + routed * (rb + 4 * K)
+        fn = lambda: moe.moe_dispatch_partitioned_ex(quant, layout, x, ids, wt, E, P, rx, rsf, rids, rw, st,
+                                                     input_global_scale=g)
+        us = timed_us(fn)
+        emit("f1", f"moe_dispatch_partitioned_ex({quant}, {layout} scales)", "nvfp4", T, us, nbytes,
+             ["dispatch_partitioned_kernel"] + (["sf_swizzle_pad_kernel"] if layout == "swizzled" else []),
+             2 if layout == "swizzled" else 1)
+        del rx, rsf, rids, rw
+    partial = torch.randn((P, S, H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    us = timed_us(lambda: moe.moe_combine_partitioned(partial, ids, E, P, out, st))
+    emit("f1", "moe_combine_partitioned", "nvfp4", T, us, routed * 2 * H + 4 * T * K + 2 * T * H,
+         ["combine_partitioned_kernel"], 1)
+    del partial, out
+
+    # f2: get_dispatch_layout outputs (decode and prefill routing, 8 partitions)
+    for name in ("decode", "prefill"):
+        w2 = make_workload(name, seed=0)
+        ids2 = torch.from_numpy(w2.topk_ids).to(dev)
+        P2 = 8
+        ntr = torch.empty(P2, dtype=torch.int32, device=dev)
+        itr = torch.empty((w2.T, P2), dtype=torch.uint8, device=dev)
+        nte = torch.empty(w2.E, dtype=torch.int32, device=dev)
+        us = timed_us(lambda: moe.moe_dispatch_layout(ids2, w2.E, P2, ntr, itr, st, nte))
+        emit("f2", "moe_dispatch_layout", name, w2.T, us, 4 * w2.T * w2.K + w2.T * P2 + 4 * P2 + 4 * w2.E,
+             ["dispatch_layout_kernel"], 1)
+
+    # f3 / f4 on the prefill workload: expert-aligned metadata from int64 ids, then the FP8
+    # dispatch with UE8M0 column-major scales into the aligned segments; FP8 pass-through rows
+    w = make_workload("prefill", seed=0)
+    x, ids, wt = dev_in(w)
+    T, H, K, E = w.T, w.H, w.K, w.E
+    A = 128
+    cap = T * K + E * (A - 1)
+    ids64 = ids.to(torch.int64)
+    seg = torch.empty(E + 1, dtype=torch.int64, device=dev)
+    s2d = torch.empty(T * K, dtype=torch.int32, device=dev)
+    reo = torch.empty(cap, dtype=torch.int32, device=dev)
+    mm = torch.empty(E, dtype=torch.int32, device=dev)
+    pc = torch.empty(8, dtype=torch.int32, device=dev)
+    i32 = torch.empty((T, K), dtype=torch.int32, device=dev)
+    ws = moe.new_workspace(T, K, E, dev)
+    fn = lambda: moe.moe_route_meta_ex(ids64, E, seg, s2d, reo, mm, st, ws, 8, 0, A, pc, topk_ids_i32_out=i32)
+    fn()
+    torch.cuda.synchronize()
+    n_rows = int(seg[-1].item())
+    n_valid = int((s2d >= 0).sum().item())
+    meta_bytes = 8 * T * K + 4 * T * K + 4 * T * K + 4 * n_rows + 8 * (E + 1) + 4 * E + 4 * 8
+    emit("f3+f4", "moe_route_meta_ex(int64 ids, expert_alignment=128, int32 copy)", "prefill", T, timed_us(fn),
+         meta_bytes, ["route_meta_count_kernel", "route_meta_place_kernel"], 2)
+    q = torch.empty((cap, H), dtype=torch.uint8, device=dev)
+    R4 = (cap + 3) // 4 * 4
+    G = H // 128
+    sc = torch.empty(((G + 3) // 4, R4, 4), dtype=torch.uint8, device=dev)
+    fn = lambda: moe.moe_dispatch_ex("normal", "fp8g128_ue8m0", "col", x, i32, E, s2d, seg, q, sc, st, out_rows=cap)
+    emit("f3", "moe_dispatch_ex(fp8g128_ue8m0, column-major scales, aligned segments)", "prefill", T,
+         timed_us(fn), 2 * T * H + 4 * T * K + n_valid * (H + G), ["dispatch_kernel"], 1)
+    codes = torch.randint(0, 256, (T, H), dtype=torch.uint8, device=dev)
+    om = moe.route_meta(ids, E, dev_status=st)
+    fn = lambda: moe.moe_dispatch_ex("normal", "fp8_passthrough", "row", codes, ids, E, om.src2dst, om.seg_indptr,
+                                     q, None, st)
+    nv = int(om.seg_indptr[-1].item())
+    emit("f4", "moe_dispatch_ex(fp8_passthrough)", "prefill", T, timed_us(fn), T * H + 4 * T * K + nv * H,
+         ["dispatch_bulk_copy_kernel"], 1)
+    del q, sc, codes
+
+    # f3: NVFP4 masked dispatch with block scales written in the 128 x 4 swizzled layout
+    w = make_workload("nvfp4", seed=0)
+    x, ids, wt = dev_in(w)
+    T, H, K, E, M = w.T, w.H, w.K, w.E, w.M
+    d = moe.MoEDispatcher(T, H, K, E, mode="masked", quant="nvfp4b16", num_partitions=w.P,
+                          max_tokens_per_expert=M, device=dev)
+    d.route(ids)
+    torch.cuda.synchronize()
+    rows = int(d.masked_m.sum().item())
+    qm = torch.empty((E, M, H // 2), dtype=torch.uint8, device=dev)
+    sfm = torch.empty((moe.swizzled_scale_bytes(E * M, H),), dtype=torch.uint8, device=dev)
+    fn = lambda: moe.moe_dispatch_ex("masked", "nvfp4b16", "swizzled", x, ids, E, d.src2dst, d.seg_indptr, qm, sfm,
+                                     st, M, input_global_scale=w.global_scale)
+    emit("f3", "moe_dispatch_ex(nvfp4b16 masked, swizzled 128x4 scales)", "nvfp4", T, timed_us(fn),
+         2 * T * H + 8 * T * K + 8 * E + rows * row_bytes("nvfp4b16", H),
+         ["dispatch_kernel", "sf_swizzle_pad_kernel"], 2)
+    torch.cuda.synchronize()
+    moe.check_status(st, "next rows")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -771,6 +931,8 @@ def main():
     ap.add_argument("--no-fuse", action="store_true", help="separate route_meta and dispatch calls")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--next-rows", action="store_true",
+                    help="instead of the step: time each NEXT-row call (one JSON line per call)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -802,6 +964,14 @@ def main():
         _build.build()
     if dist:
         dist.barrier()
+
+    if args.next_rows:
+        if rank == 0:
+            run_next_rows(args)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
 
     w = make_workload(args.workload, seed=rank_seed(rank))
     cpu = cpu_all = None
