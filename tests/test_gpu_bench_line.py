@@ -43,3 +43,18 @@ def test_reference_arm_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_next_rows_lines():
+    """bench.py --next-rows: one well-formed line per NEXT-row call (f1-f4), each a positive time
+    and a fraction equal to GB/s over the peak."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--next-rows", "--steps", "3",
+                          "--warmup", "3"], capture_output=True, text=True, cwd=ROOT, timeout=900)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [json.loads(l) for l in out.stdout.splitlines() if l.strip().startswith("{")]
+    assert {d["row"] for d in lines} == {"f1", "f2", "f3", "f4", "f3+f4"}
+    for d in lines:
+        assert d["us"] > 0 and d["algorithmic_bytes"] > 0 and d["peak"] > 0
+        assert abs(d["gbs"] - d["algorithmic_bytes"] / d["us"] / 1e3) < 1e-6 * d["gbs"]
+        assert abs(d["frac"] - d["gbs"] / d["peak"]) < 1e-9
+        assert d["kernels"] and d["launches_per_call"] >= 1
