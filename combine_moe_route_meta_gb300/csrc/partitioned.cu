@@ -14,10 +14,12 @@
 //   combine sums, per token, the (already weighted) partial outputs of the partitions the
 //   token was sent to.
 //
-// Design: the same warp-per-(token, 512-column slice) structure as dispatch.cu / combine.cu.
-// Lanes 0..K-1 hold the token's expert ids; lane p (< P <= 32) tests every id against its
-// partition's expert range, so the destination row of lane p is p*num_slots + t or -1,
-// and the row broadcast of the shared quantise_store serves P candidate rows.
+// Design: batches of at least 1024 tokens whose rows suit whole-row bulk copies go to the
+// bulk (TMA) dispatch kernels of dispatch.cu with partition destinations. Smaller ones, and
+// the combine, use the same warp-per-(token, 512-column slice) structure as dispatch.cu /
+// combine.cu. Lanes 0..K-1 hold the token's expert ids; lane p (< P <= 32) tests every id
+// against its partition's expert range, so the destination row of lane p is p*num_slots + t
+// or -1, and the row broadcast of the shared quantise_store serves P candidate rows.
 #include <cstdint>
 
 #include "dispatch_slice.cuh"
