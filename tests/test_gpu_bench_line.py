@@ -38,13 +38,6 @@ def test_bench_line_has_the_contract_keys():
     assert set(d["graph_replay"]) >= {"cold_l2", "warm_l2"}
 
 
-def test_reference_arm_line():
-    d = _run("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3")
-    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
-    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
-
-
 def test_next_rows_lines():
     """bench.py --next-rows: one well-formed line per NEXT-row call (f1-f4), each a positive time
     and a fraction equal to GB/s over the peak."""
