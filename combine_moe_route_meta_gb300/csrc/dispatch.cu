@@ -208,6 +208,7 @@ struct BulkGeom {
     uint32_t in_off;     // shared offsets
     uint32_t out_off;
     int stages;
+    int ts;  // scales stored by the threads (TS kernels), s_bytes then only sizes the staging
 };
 
 constexpr int kBulkCopyThreads = 32;
@@ -219,6 +220,48 @@ template <bool MASKED>
 __device__ __forceinline__ void stage_seg(const DispatchArgs& a, int* s_seg) {
     if (MASKED)
         stage_to_shared(a.seg, s_seg, a.E);
+}
+
+// TS kernels: the staged scale row `so` of the current token, written by all threads to each
+// destination row in rows[0..nd) (< 0: none) in the output's scale layout. Swizzled NVFP4:
+// 4 consecutive columns of a row are 4 contiguous bytes of the 128 x 4 tile layout, so each
+// row takes H/64 word stores. FP8 fp32 scales: one word per group (column-major, or a
+// row-major array whose rows are not 16-byte multiples). UE8M0 and row-major NVFP4 scales:
+// one byte per group, at the index the register path writes.
+template <int QUANT>
+__device__ __forceinline__ void store_scales_from_stage(const DispatchArgs& a, const unsigned char* so,
+                                                        const int64_t* rows, int nd, int H, int tid, int nthreads) {
+    uint8_t* out = static_cast<uint8_t*>(a.out_s);
+    if constexpr (QUANT == MOE_QUANT_NVFP4_B16) {
+        if (a.L.kind == MOE_SCALES_SWIZZLED_128X4) {
+            const int C4 = H / 64;
+            for (int j = tid; j < nd * C4; j += nthreads) {
+                const int k = j / C4, c4 = j - k * C4;
+                const int64_t row = rows[k];
+                if (row >= 0)
+                    *reinterpret_cast<uint32_t*>(out + swizzled_128x4_index(row, 4 * c4, H / 16)) =
+                        *reinterpret_cast<const uint32_t*>(so + 4 * c4);
+            }
+            return;
+        }
+    }
+    if constexpr (QUANT == MOE_QUANT_FP8_G128) {
+        const int G = H / 128;
+        for (int j = tid; j < nd * G; j += nthreads) {
+            const int k = j / G, g = j - k * G;
+            const int64_t row = rows[k];
+            if (row >= 0)
+                reinterpret_cast<uint32_t*>(out)[scale_index(a.L, row, g, G, false)] =
+                    reinterpret_cast<const uint32_t*>(so)[g];
+        }
+    } else {
+        const int G = QUANT == MOE_QUANT_NVFP4_B16 ? H / 16 : H / 128;
+        for (int j = tid; j < nd * G; j += nthreads) {
+            const int k = j / G, g = j - k * G;
+            const int64_t row = rows[k];
+            if (row >= 0) out[scale_index(a.L, row, g, G, true)] = so[g];
+        }
+    }
 }
 
 // copy mode: lane 0 drives the ring, lanes < K (partitions < P) resolve the destination rows
@@ -282,7 +325,7 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
 }
 
 // quantising modes: 256 threads quantise shared -> shared; thread 0 drives the copies
-template <int QUANT, bool MASKED, bool PART, bool SWZ>
+template <int QUANT, bool MASKED, bool PART, bool TS>
 __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(DispatchArgs a, BulkGeom geo) {
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait();
@@ -361,32 +404,19 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
         }
         fence_proxy_async();
         __syncthreads();
-        // SWZ (NVFP4 only): scales in the 128 x 4 tile layout, stored by the threads below
-        constexpr bool swizzled = SWZ && QUANT == MOE_QUANT_NVFP4_B16;
+        // TS: the scale rows are stored by the threads below (layouts a bulk row cannot write)
         if (tid == 0) {
             for (int k = 0; k < nd; k++) {
                 const int64_t row = s_rows[o * kBulkRows + k];
                 if (row < 0) continue;
                 bulk_store(static_cast<uint8_t*>(a.out_q) + row * geo.q_bytes, out0 + o * out_bytes, geo.q_bytes);
-                if (!swizzled)
+                if (!TS)
                     bulk_store(static_cast<uint8_t*>(a.out_s) + row * geo.s_bytes, out0 + o * out_bytes + geo.q_bytes,
                                geo.s_bytes);
             }
             bulk_commit();
         }
-        if constexpr (swizzled) {
-            // block scales in the 128 x 4 tile layout: 4 consecutive columns of a row are 4
-            // contiguous bytes, so every destination row takes C/4 word stores from the staged row
-            const int C4 = H / 64;
-            for (int j = tid; j < nd * C4; j += nthreads) {
-                const int k = j / C4, c4 = j - k * C4;
-                const int64_t row = s_rows[o * kBulkRows + k];
-                if (row >= 0)
-                    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.out_s) +
-                                                 swizzled_128x4_index(row, 4 * c4, H / 16)) =
-                        *reinterpret_cast<const uint32_t*>(so + 4 * c4);
-            }
-        }
+        if constexpr (TS) store_scales_from_stage<QUANT>(a, so, s_rows + o * kBulkRows, nd, H, tid, nthreads);
     }
     if (tid == 0) {
         bulk_wait_all();
@@ -407,13 +437,16 @@ BulkGeom bulk_geometry(int quant, const DispatchArgs& a) {
         case MOE_QUANT_FP8_G128_UE8M0: g.q_bytes = uint32_t(H); g.s_bytes = uint32_t(H / 128); break;
         default: g.q_bytes = uint32_t(H / 2); g.s_bytes = uint32_t(H / 16); break;
     }
-    // swizzled NVFP4 scales are written in 4-byte pieces by the threads (not as a bulk row),
-    // so only the row-major scale array needs a 16-byte aligned base
-    const bool swizzled = a.L.kind == MOE_SCALES_SWIZZLED_128X4 && quant == MOE_QUANT_NVFP4_B16;
+    // A scale row goes out as one bulk store when it is row-major, a 16-byte multiple and
+    // 16-byte aligned; otherwise (swizzled or column-major layouts, short or unaligned rows)
+    // the threads store it (TS) and s_bytes only sizes its staging, rounded up to 16 bytes so
+    // that every stage's code row stays 16-byte aligned for its bulk store.
     const bool aligned16 = (reinterpret_cast<uintptr_t>(a.out_s) & 15) == 0;
-    if (g.q_bytes % 16 || g.s_bytes % 16 || (a.L.kind != MOE_SCALES_ROW_MAJOR && !swizzled) ||
-        (quant != MOE_QUANT_NONE && !swizzled && !aligned16))
-        return g;
+    const bool ts = quant != MOE_QUANT_NONE &&
+                    (a.L.kind != MOE_SCALES_ROW_MAJOR || g.s_bytes % 16 != 0 || !aligned16);
+    if (g.q_bytes % 16) return g;
+    if (ts) g.s_bytes = (g.s_bytes + 15) / 16 * 16;
+    g.ts = ts;
     const uint32_t seg_bytes = uint32_t(sizeof(int)) * uint32_t(a.E);
     // ring depth, measured on GB300 (prefill / qwen3 / nvfp4 shapes): the copy mode is flat
     // from 2 to 6 stages; FP8 is best at 3; NVFP4 is best at 2, where its smaller footprint
@@ -446,9 +479,8 @@ cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkG
         const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1)));
         return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
     } else {
-        auto kern = dispatch_bulk_quant_kernel<QUANT, MASKED, PART, false>;
-        if constexpr (QUANT == MOE_QUANT_NVFP4_B16)
-            if (a.L.kind == MOE_SCALES_SWIZZLED_128X4) kern = dispatch_bulk_quant_kernel<QUANT, MASKED, PART, true>;
+        auto kern = geo.ts ? dispatch_bulk_quant_kernel<QUANT, MASKED, PART, true>
+                           : dispatch_bulk_quant_kernel<QUANT, MASKED, PART, false>;
         // as many passes over the row's 16-element slices as 256 threads need, with the block
         // sized so that every pass is full (H = 7168: 448 slices = 2 x 224, not 256 + 192)
         const int nslices = a.H / kLaneElems;

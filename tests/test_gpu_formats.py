@@ -54,12 +54,14 @@ def _colmajor_ue8m0(rowmajor, R4):
     return out
 
 
+@pytest.mark.parametrize("T", [300, 1100])   # register path; bulk kernel with thread-stored scales
 @pytest.mark.parametrize("quant", ["fp8g128", "fp8g128_ue8m0"])
 @pytest.mark.parametrize("layout", ["row", "col"])
-def test_aligned_dispatch_and_combine(quant, layout):
-    """Normal layout over 128-aligned segments, both scale layouts."""
+def test_aligned_dispatch_and_combine(quant, layout, T):
+    """Normal layout over 128-aligned segments, both scale layouts (H = 640: 5 groups, so
+    neither scale row is a 16-byte multiple)."""
     m = moe()
-    T, H, E, K, A = 300, 640, 24, 6, 128
+    H, E, K, A = 640, 24, 6, 128
     w = make_case(T, H, E, K, seed=51, routing="zipf", invalid_rate=0.05)
     x, ids, wt = to_dev(w)
     cap = T * K + E * (A - 1)
@@ -122,11 +124,12 @@ def test_aligned_dispatch_and_combine(quant, layout):
     assert int(st.item()) == 0
 
 
+@pytest.mark.parametrize("T,M", [(96, 30), (1100, 300)])   # register path; bulk kernel
 @pytest.mark.parametrize("quant", ["fp8g128", "fp8g128_ue8m0"])
-def test_masked_colmajor_scales(quant):
+def test_masked_colmajor_scales(quant, T, M):
     """Masked layout [E, M, .] with per-expert column-major scales [E, G, roundup(M, 4)]."""
     m = moe()
-    T, H, E, K, M = 96, 1024, 16, 4, 30
+    H, E, K = 1024, 16, 4
     w = make_case(T, H, E, K, seed=53, invalid_rate=0.05)
     x, ids, _ = to_dev(w)
     om = oracle.route_meta(w.topk_ids, E, M=M)
@@ -264,7 +267,7 @@ def test_ue8m0_bulk_path_normal_layout():
     ("masked", 96, 1024, 16, 4, 30),     # E*M = 480 rows -> padded to 512
     ("masked", 128, 7168, 256, 8, 128),  # the decode shape: 32768 rows, no padding
     ("masked", 1100, 7168, 64, 8, 200),  # bulk kernel, masked rows
-    ("masked", 1100, 1088, 64, 8, 200),  # H % 256 != 0: swizzled scales from the register path
+    ("masked", 1100, 1088, 64, 8, 200),  # H % 256 != 0: the bulk kernel still stores the swizzled words
 ])
 def test_nvfp4_swizzled_scales_match_oracle_interleave(mode, T, H, E, K, M):
     """The whole scale buffer equals the oracle's row-major scales (untouched rows keep

@@ -52,7 +52,7 @@ def test_dispatch_layout_matches_oracle(T, E, K, P, bad):
     (1100, 1200, 2048, 64, 8, 8, "nvfp4b16", -1),   # padding slots
     (1030, 1030, 512, 32, 4, 4, "none", 32),        # invalid id = E
     (2000, 2050, 256, 64, 16, 32, "nvfp4b16", -1),  # K = 16, P = 32
-    (1024, 1024, 1088, 16, 2, 2, "nvfp4b16", -1),   # H % 256 != 0: NVFP4 stays on the register path
+    (1024, 1024, 1088, 16, 2, 2, "nvfp4b16", -1),   # H % 256 != 0: bulk kernel, scale bytes stored by its threads
 ])
 def test_partitioned_dispatch_and_combine_match_oracle(T, S, H, E, K, P, quant, inv):
     m = moe()
