@@ -1,4 +1,5 @@
-// moe_abi.cu -- the extern "C" entry points declared in include/moe_dispatch.h.
+// moe_abi.cu -- the extern "C" entry points declared in include/moe_dispatch.h (the hot path)
+// and include/moe_diag.h (test hooks).
 //
 // Each entry point validates its arguments on the host (returning a status and launching
 // nothing on failure), reads the SM count of the current device, and hands the launch to
@@ -7,6 +8,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "moe_diag.h"
 #include "moe_dispatch.h"
 #include "moe_launch.h"
 

@@ -96,7 +96,7 @@ struct RoutePlan {
     bool single;
     int rounds;        // R: rounds of 32 pairs per warp
     int blocks;        // B
-    size_t ws_bytes;   // scratch: ticket + per-block count table [B][E]
+    size_t ws_bytes;   // scratch: the per-block count table [B][E] (int32)
 };
 RoutePlan plan_route_meta(int64_t n_pairs, int num_experts);
 

@@ -37,9 +37,6 @@ namespace {
 
 constexpr int kWarps = kRouteThreads / 32;
 
-// workspace layout: a 256-byte reserved header, then the int32 table [B][E]
-constexpr size_t kTableOffset = 256;
-
 // Block-wide exclusive scan of one int per thread (blockDim == 1024).
 // `warp_sums` is 32 ints of shared memory. Returns the exclusive prefix; *total gets the sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
@@ -450,7 +447,9 @@ RoutePlan plan_route_meta(int64_t n_pairs, int num_experts) {
     p.single = false;
     p.rounds = int(R);
     p.blocks = int((n_pairs + chunk - 1) / chunk);
-    p.ws_bytes = kTableOffset + sizeof(int32_t) * size_t(p.blocks) * size_t(num_experts);
+    // the workspace is the int32 table [B][E]; every block writes its whole row before the
+    // place kernel reads any of it, so the table needs no initial contents
+    p.ws_bytes = sizeof(int32_t) * size_t(p.blocks) * size_t(num_experts);
     return p;
 }
 
@@ -476,7 +475,7 @@ cudaError_t launch_route_meta(const LaunchCtx& ctx, const RoutePlan& plan, const
     a.masked_m = masked_m;
     a.partition_counts = partition_counts;
     a.status = dev_status;
-    if (!plan.single) a.table = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kTableOffset);
+    if (!plan.single) a.table = static_cast<int32_t*>(workspace);
     if (plan.rounds <= 1) return launch_rmax<1>(ctx, plan, a, E);
     if (plan.rounds <= 2) return launch_rmax<2>(ctx, plan, a, E);
     if (plan.rounds <= 4) return launch_rmax<4>(ctx, plan, a, E);

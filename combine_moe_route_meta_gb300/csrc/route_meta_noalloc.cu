@@ -1,7 +1,7 @@
 // route_meta_noalloc.cu -- moe_route_meta for callers that cannot allocate device memory.
 //
 // moe_route_meta needs a caller-provided scratch buffer once the pairs span several
-// thread blocks (a per-block histogram table plus a reserved header). Some callers
+// thread blocks (the per-block histogram table [B][E]). Some callers
 // have no way to provide one: an inference engine that has already reserved the GPU's
 // memory for its own pool, a plugin interface that passes in nothing but input and
 // output pointers, or a code path where a cudaMalloc (which can synchronise the device)
@@ -12,8 +12,9 @@
 // that loads the library holds it until the process exits. Its device address is looked
 // up once per device, with that device current, on the first call made on that device.
 // All calls share the array, so calls whose kernels overlap on the GPU race with each
-// other; the part that must start at zero (the reserved header) is cleared on the stream before
-// every call. No call allocates or frees memory.
+// other. Nothing in it has to start at zero: the count kernel writes every table cell the
+// place kernel reads, so a call never sees what an earlier call left there. No call
+// allocates or frees memory, and no call issues anything but the kernels of moe_route_meta.
 #include <cstdint>
 #include <mutex>
 
@@ -24,7 +25,6 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(1) << 20;  // 1 MiB
-constexpr size_t kHeaderBytes = 256;                      // header that must start zeroed
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocScratchBytes];
@@ -63,8 +63,6 @@ extern "C" moe_status_t moe_route_meta_noalloc(const int32_t* topk_ids, int64_t 
     if (need > 0) {
         moe_status_t st = scratch_address(&scratch);
         if (st != MOE_OK) return st;
-        if (cudaMemsetAsync(scratch, 0, kHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-            return MOE_ERR_CUDA;
     }
     return moe_route_meta(topk_ids, num_tokens, topk, num_experts, num_partitions, max_tokens_per_expert,
                           seg_indptr, src2dst, reorder_topk_ids, masked_m, partition_counts, expected_m_host,

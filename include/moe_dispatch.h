@@ -103,9 +103,11 @@ const char *moe_status_string(moe_status_t status);
 
 /*
  * Bytes of scratch that moe_route_meta needs for num_tokens x topk pairs and
- * num_experts experts (0 when one thread block handles all pairs). The workspace
- * must be zero-filled once when it is allocated; every call that completes leaves
- * it ready for the next call. Calls that share a workspace must not overlap on the GPU.
+ * num_experts experts (0 when one thread block handles all pairs, i.e. up to 2048 pairs).
+ * The scratch holds one int32 histogram row per thread block of the count kernel
+ * ([B][E], B = the block count); each call writes every row before it reads any, so
+ * its initial contents do not matter (no clearing, neither at allocation nor per call).
+ * Calls that share a workspace must not overlap on the GPU.
  * Returns 0 for arguments moe_route_meta would reject.
  */
 size_t moe_route_meta_workspace_size(int64_t num_tokens, int topk, int num_experts);
@@ -141,8 +143,8 @@ size_t moe_route_meta_workspace_size(int64_t num_tokens, int topk, int num_exper
  *   masked_m            [E] int32 out.
  *   partition_counts    [P] int32 out, or NULL.
  *   expected_m_host     host int32 out, or NULL.
- *   workspace           moe_route_meta_workspace_size(T, K, E) bytes, zero-filled at
- *                       allocation; may be NULL when that size is 0.
+ *   workspace           moe_route_meta_workspace_size(T, K, E) bytes, 256-byte aligned
+ *                       (as cudaMalloc returns), any contents; may be NULL when that size is 0.
  *   dev_status          [1] int32 device status word (see conventions).
  * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
  */
@@ -194,14 +196,14 @@ moe_status_t moe_route_meta_ex(const void *topk_ids, int topk_ids_bytes, int64_t
  * Scratch: a fixed 1 MiB array in the library's own device memory (every GPU that loads
  * the library holds it until the process exits). Sizes whose moe_route_meta workspace
  * would exceed 1 MiB are rejected with MOE_ERR_UNSUPPORTED before anything is launched:
- * with 1024 experts it covers up to 4,177,920 (token, k) pairs, with 256 experts up to
- * 16,760,832. Up to 2048 pairs need no scratch at all.
+ * with 1024 experts it covers up to 4,194,304 (token, k) pairs, with 256 experts up to
+ * 16,777,216, with 128 experts up to 33,554,432. Up to 2048 pairs need no scratch at all.
  * First call on a device: looks up the array's device address with that device current;
- * make that first call before any stream capture. Each call clears the scratch header
- * with a cudaMemsetAsync on `stream` before its kernels.
- * Every call shares the one array, which keeps the previous call's contents: calls whose
- * kernels may overlap on the GPU (different streams, no ordering between them) race and
- * must not be issued.
+ * make that first call before any stream capture. A call issues exactly the kernels of
+ * moe_route_meta and nothing else (no memset, no copy).
+ * Every call shares the one array, which keeps the previous call's contents (no call
+ * depends on them: each writes every cell it reads). Calls whose kernels may overlap on
+ * the GPU (different streams, no ordering between them) race and must not be issued.
  * Returns the statuses of moe_route_meta.
  */
 moe_status_t moe_route_meta_noalloc(const int32_t *topk_ids, int64_t num_tokens, int topk,
@@ -291,7 +293,7 @@ moe_status_t moe_dispatch_ex(moe_mode_t mode, moe_quant_t quant, moe_scale_layou
  * normal mode, where M > 0 only enables the capacity check of masked_m).
  * Small batches (T <= 512 and T*K <= 4096 pairs) run as a single kernel that needs no
  * workspace (workspace may be NULL); larger ones need moe_route_meta_workspace_size(T, K, E)
- * bytes of zero-filled workspace, exactly as moe_route_meta.
+ * bytes of workspace, exactly as moe_route_meta.
  * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED or MOE_ERR_CUDA.
  */
 moe_status_t moe_route_dispatch(moe_mode_t mode, moe_quant_t quant, const uint16_t *hidden_states,
@@ -408,56 +410,6 @@ moe_status_t moe_dispatch_partitioned_ex(moe_quant_t quant, moe_scale_layout_t s
 moe_status_t moe_combine_partitioned(const uint16_t *partial, int64_t num_tokens, int64_t num_slots, int hidden,
                                      const int32_t *topk_ids, int topk, int num_experts, int num_partitions,
                                      uint16_t *out, int32_t *dev_status, moe_stream_t stream);
-
-/*
- * moe_fp8_division_check -- diagnostics: the FP8 quantiser divides by its group scale with
- * the scale's reciprocal and one correction step (after Markstein) instead of a division per
- * element. This call checks that choice exhaustively on the GPU: for every non-negative finite
- * bf16 amax (0 clamped to 1e-10), s = amax/448, and every bf16 x with |x| <= amax, it compares
- * the result with the IEEE division.
- * (No counterpart on the pages: a test hook for sglang_per_token_group_quant_fp8's x / s.)
- *   result  [4] uint64 device out (cleared on `stream` first):
- *           [0] pairs whose e4m3 codes differ, [1] the first one as (x bits << 32) | s bits,
- *           [2] pairs whose quotients differ while |x / s| >= 2^-12,
- *           [3] pairs whose quotients differ at all (expected only for |x| < 2^-103, where the
- *               correction's remainder leaves the normal range and the code is a zero anyway).
- * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
- */
-moe_status_t moe_fp8_division_check(unsigned long long *result, moe_stream_t stream);
-
-/*
- * moe_wait_timeout_check -- diagnostics: runs the bounded wait of the bulk (TMA) dispatch
- * kernels on one shared-memory mbarrier of arrival count 1, so that its give-up path can be
- * checked without any fault. With complete = 1 the kernel arrives at the barrier first and
- * the wait returns at once; with complete = 0 nothing ever arrives, the wait gives up after
- * limit_ns of wall-clock time and the kernel writes MOE_ERR_TIMEOUT to dev_status (first
- * error wins) and exits. The dispatch kernels wait the same way with a limit of 1 s per ring
- * stage (0.1 s for draining their loads after a timeout).
- * (No counterpart on the pages: a test hook for the library's own bounded waits.)
- *   dev_status  [1] int32 device status word.
- *   limit_ns    1 .. 10^10.
- *   complete    0 or 1.
- * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
- */
-moe_status_t moe_wait_timeout_check(int32_t *dev_status, int64_t limit_ns, int complete, moe_stream_t stream);
-
-/*
- * moe_convert_probe -- diagnostics: run the number-format conversions of the quantising
- * kernels on arbitrary fp32 inputs, so their rounding, saturation, signed zeros and
- * packing order can be checked against an independent implementation of the formats.
- * (No counterpart on the pages: a test hook for the e4m3 / e2m1 codecs used by
- * sglang_per_token_group_quant_fp8 and fp4_quantize.)
- *   in          [n] fp32, n even.
- *   e4m3        [n] uint8 out: e4m3_rn_satfinite(in[j]), converted in pairs
- *               (in[2j], in[2j+1]) exactly as the FP8 kernel packs them; or NULL.
- *   e2m1        [n/2] uint8 out: byte j = e2m1(in[2j]) | e2m1(in[2j+1]) << 4, as the NVFP4
- *               kernel packs them; or NULL.
- *   e4m3_value  [n] fp32 out: the value of the e4m3 code of in[j], decoded as the NVFP4
- *               kernel decodes its block scales; or NULL.
- * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
- */
-moe_status_t moe_convert_probe(const float *in, int64_t n, uint8_t *e4m3, uint8_t *e2m1,
-                               float *e4m3_value, moe_stream_t stream);
 
 /*
  * moe_combine_ex -- moe_combine with the row capacity of expert_out in the normal layout

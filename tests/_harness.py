@@ -158,9 +158,33 @@ def run_full(w: Workload, *, expert_seed: int = 1234, check_untouched: bool = Tr
     return om
 
 
-def run_sampled(w: Workload, *, n_sample: int = 256, expert_seed: int = 4321, sample_seed: int = 7):
-    """Full-size workload in the benchmark's launch configuration: metadata compared in full,
-    dispatch and combine compared on a seeded sample of tokens (all K rows of each)."""
+def _sentinel_buffer(shape, dtype) -> torch.Tensor:
+    """A device buffer of `shape` whose every byte is SENTINEL."""
+    n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+    return torch.full((n,), SENTINEL, dtype=torch.uint8, device="cuda").view(dtype).view(shape)
+
+
+def _all_bytes_are(t2d: torch.Tensor, value: int, chunk_bytes: int = 1 << 30) -> bool:
+    """Every byte of a [rows, bytes] uint8 device tensor equals `value` (checked in row chunks,
+    so no temporary the size of a multi-GB buffer is made)."""
+    rows = max(1, chunk_bytes // max(1, t2d.shape[1]))
+    for r0 in range(0, t2d.shape[0], rows):
+        if bool((t2d[r0:r0 + rows] != value).any()):
+            return False
+    return True
+
+
+def run_full_large(w: Workload, *, expert_seed: int = 4321):
+    """A full-size workload in the benchmark's launch configuration, compared in full.
+
+    Metadata: every entry. Dispatch: every written row and scale row, bit for bit, against
+    the oracle's rows in src2dst order (the contiguous layout: out[src2dst[i]] = Q(x[t]));
+    in the masked layout each row e*M + rank is the contiguous row seg_indptr[e] + rank by
+    definition, so the GPU's masked rows are gathered into that order on the device first.
+    Every other row of the output (beyond N, or at slots >= masked_m[e]) must still hold the
+    sentinel fill. Combine: every element of every token, against the oracle's binary64 sum
+    over the compact expert rows (the masked buffer holds the same rows at e*M + rank).
+    The host never materialises the [E, M, .] buffers, which run to tens of GB."""
     m = moe()
     x, ids, wt = to_dev(w)
     om = oracle.route_meta(w.topk_ids, w.E, P=w.P, M=w.M)
@@ -170,58 +194,56 @@ def run_sampled(w: Workload, *, n_sample: int = 256, expert_seed: int = 4321, sa
     assert om.status == 0
 
     qs, qd, ss, sd = m.dispatch_out_shapes(w.mode, w.quant, w.T, w.H, w.K, w.E, w.M)
-    q = torch.empty(qs, dtype=qd, device="cuda")
-    s = torch.empty(ss, dtype=sd, device="cuda") if ss is not None else None
+    q = _sentinel_buffer(qs, qd)
+    s = _sentinel_buffer(ss, sd) if ss is not None else None
     st2 = m.new_status()
     m.moe_dispatch(w.mode, w.quant, x, ids, w.E, gm.src2dst, gm.seg_indptr, q, s, st2, w.M,
                    w.global_scale or 0.0)
 
-    rows = om.src2dst.astype(np.int64) if w.mode == "normal" else masked_rows(w, om)
     n = om.num_valid
-    # compact expert outputs, row j belongs to the pair with src2dst == j
-    rng = np.random.default_rng(expert_seed)
-    eo_compact = random_bf16(rng, (n, w.H))
-    pair_of_slot = np.empty(n, np.int64)
     valid = om.src2dst >= 0
+    pair_of_slot = np.empty(n, np.int64)
     pair_of_slot[om.src2dst[valid]] = np.nonzero(valid)[0]
+    rows = om.src2dst.astype(np.int64) if w.mode == "normal" else masked_rows(w, om)
+    dst = rows[pair_of_slot]                      # output row of contiguous slot j
+    assert (dst >= 0).all()                       # no capacity drops in these workloads
+
+    # oracle: the contiguous layout of all N rows
+    oq, osc = oracle.dispatch("normal", w.quant, w.x, w.topk_ids, om, w.E, global_scale=w.global_scale or 0.0,
+                              rows=max(n, 1))
+    q2 = q.view(torch.uint8).view(int(np.prod(qs[:-1])), -1)
+    dst_d = torch.from_numpy(dst).cuda()
+    got_rows = q2.index_select(0, dst_d)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    assert np.array_equal(got_rows.cpu().numpy(), np.ascontiguousarray(oq[:n]).view(np.uint8).reshape(n, -1)), \
+        "dispatch rows"
+    # the written rows are checked: overwrite them with the fill, then every byte must be the fill
+    q2.index_fill_(0, dst_d, SENTINEL)
+    assert _all_bytes_are(q2, SENTINEL), "rows no pair maps to were written"
+    if s is not None:
+        s2 = s.view(torch.uint8).view(q2.shape[0], -1)
+        got_sc = s2.index_select(0, dst_d)
+        assert np.array_equal(got_sc.cpu().numpy(), np.ascontiguousarray(osc[:n]).view(np.uint8).reshape(n, -1)), \
+            "dispatch scales"
+        s2.index_fill_(0, dst_d, SENTINEL)
+        assert _all_bytes_are(s2, SENTINEL), "scale rows no pair maps to were written"
+    del q, s, q2, got_rows
+
+    # combine over compact expert rows (row j of eo_compact is the expert output of slot j)
+    rng = np.random.default_rng(expert_seed)
+    eo_compact = random_bf16(rng, (max(n, 1), w.H))
+    eo_c = torch.from_numpy(eo_compact.view(np.int16)).cuda().view(torch.bfloat16)
     if w.mode == "normal":
-        eo = torch.from_numpy(eo_compact.view(np.int16)).cuda().view(torch.bfloat16)
+        eo = eo_c
     else:
         eo = torch.zeros((w.E * w.M, w.H), dtype=torch.bfloat16, device="cuda")
-        dst = torch.from_numpy(rows[pair_of_slot]).cuda()
-        eo.index_copy_(0, dst, torch.from_numpy(eo_compact.view(np.int16)).cuda().view(torch.bfloat16))
-    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+        eo.index_copy_(0, dst_d, eo_c[:n])
+    out = filled((w.T, w.H), torch.bfloat16)
     st3 = m.new_status()
     m.moe_combine(w.mode, eo, ids, wt, w.E, gm.src2dst, gm.seg_indptr, out, st3, w.M)
+    want = oracle.combine("normal", eo_compact, w.topk_ids, w.topk_weights, om, w.E)
     torch.cuda.synchronize()
-    assert int(st2.item()) == 0 and int(st3.item()) == 0
-
-    srng = np.random.default_rng(sample_seed)
-    tokens = np.unique(np.concatenate([[0, w.T - 1], srng.choice(w.T, size=min(n_sample, w.T), replace=False)]))
-    q2 = q.view(-1, q.shape[-1])
-    s2 = s.view(-1, s.shape[-1]) if s is not None else None
-    for t in tokens:
-        t = int(t)
-        if w.quant == "fp8g128":
-            oq, os_ = oracle.quant_fp8_row(w.x[t])
-        elif w.quant == "nvfp4b16":
-            oq, os_ = oracle.quant_nvfp4_row(w.x[t], w.global_scale)
-        else:
-            oq, os_ = w.x[t].view(np.uint8), None
-        for k in range(w.K):
-            r = int(rows[t * w.K + k])
-            if r < 0:
-                continue
-            assert np.array_equal(q2[r].view(torch.uint8).cpu().numpy(), np.ascontiguousarray(oq).view(np.uint8)), (t, k)
-            if os_ is not None:
-                assert np.array_equal(s2[r].view(torch.uint8).cpu().numpy(), np.ascontiguousarray(os_).view(np.uint8)), (t, k)
-    # combine: the oracle on the sampled tokens (normal layout over the compact rows)
-    sub_ids = w.topk_ids[tokens]
-    sub_w = w.topk_weights[tokens]
-    sub_s2d = om.src2dst.reshape(w.T, w.K)[tokens].reshape(-1)
-    sub_meta = oracle.Meta(om.seg_indptr, np.ascontiguousarray(sub_s2d), om.reorder_topk_ids, om.masked_m,
-                           om.partition_counts, om.expected_m, 0)
-    want = oracle.combine("normal", eo_compact, sub_ids, sub_w, sub_meta, w.E)
-    got = out[torch.from_numpy(tokens).cuda()].contiguous()
-    check_combine(bytes_of(got).view(np.uint16).reshape(len(tokens), w.H), want)
-    return om, q, s, out
+    assert int(st3.item()) == 0
+    check_combine(bytes_of(out).view(np.uint16).reshape(w.T, w.H), want)
+    return om

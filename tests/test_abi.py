@@ -36,6 +36,17 @@ def test_header_declares_the_three_calls():
         assert n in names, names
 
 
+def test_diagnostics_live_in_their_own_header():
+    """The hot-path boundary (moe_dispatch.h) declares no test hook; moe_diag.h holds them."""
+    def declared(name):
+        src = open(os.path.join(ROOT, "include", name)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        return set(re.findall(r"\b(moe_\w+)\s*\(", src))
+    diag = {"moe_convert_probe", "moe_fp8_division_check", "moe_wait_timeout_check"}
+    assert diag <= declared("moe_diag.h")
+    assert not diag & declared("moe_dispatch.h")
+
+
 def test_library_exports_every_declared_symbol(lib):
     from combine_moe_route_meta_gb300 import build
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True, text=True).stdout
@@ -56,7 +67,7 @@ def test_workspace_size_is_host_only():
     import combine_moe_route_meta_gb300 as moe
     assert moe.moe_route_meta_workspace_size(128, 8, 256) == 0          # one block
     n = moe.moe_route_meta_workspace_size(16384, 8, 128)                # 128 blocks x 128 experts
-    assert n == 256 + 4 * 128 * 128
+    assert n == 4 * 128 * 128                                           # int32 [B][E], nothing else
     assert moe.moe_route_meta_workspace_size(10, 17, 8) == 0            # K too large -> rejected
     assert moe.moe_route_meta_workspace_size(-1, 8, 8) == 0
 

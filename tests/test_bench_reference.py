@@ -22,3 +22,17 @@ def test_reference_arm_line():
     assert d["steps"] == 2 and d["warmup"] == 3 and d["config"]["workload"] == "tiny"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    # the GPU arm prints the same config dict for the same workload (run facts live elsewhere)
+    sys.path.insert(0, ROOT)
+    import bench
+    from workloads import make_workload
+    assert d["config"] == bench.config_of(make_workload("tiny"))
+
+
+def test_default_workload_is_the_largest_config():
+    """With no flags the benchmark's headline is the Qwen3-MoE-like batch (the largest shape)."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, cwd=ROOT, timeout=900)
+    assert out.returncode == 0, out.stderr[-2000:]
+    d = json.loads([l for l in out.stdout.splitlines() if l.strip().startswith("{")][0])
+    assert d["config"]["workload"] == "qwen3" and d["config"]["T"] == 16384 and d["config"]["H"] == 4096

@@ -22,7 +22,7 @@ def _run(*args):
 
 
 def test_bench_line_has_the_contract_keys():
-    d = _run("--workload", "tiny", "--steps", "4", "--warmup", "3", "--no-cpu-baseline")
+    d = _run("--workload", "tiny", "--per-config", "none", "--steps", "4", "--warmup", "3", "--no-cpu-baseline")
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
               "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"):
         assert k in d, k
@@ -36,6 +36,25 @@ def test_bench_line_has_the_contract_keys():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] == 64 * 256 * 2
     assert d["gpu_launches"] == 4 * 2                 # fused route+dispatch, then combine
     assert set(d["graph_replay"]) >= {"cold_l2", "warm_l2"}
+
+
+def test_per_config_entries():
+    """--per-config: each listed workload gets an entry measured in the same run, with its own
+    config (the one the reference arm prints for it), step time, roofline and e2e."""
+    import bench
+    from workloads import make_workload
+    d = _run("--workload", "tiny", "--per-config", "decode", "--steps", "3", "--warmup", "3", "--no-cpu-baseline")
+    assert set(d["per_config"]) == {"decode"}
+    p = d["per_config"]["decode"]
+    assert p["config"] == bench.config_of(make_workload("decode"))
+    assert p["value"] > 0 and p["ms_per_step"] > 0 and p["unit"] == "tokens/s"
+    r = p["roofline"]
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert abs(r["frac_vs_8tbs"] - r["achieved"] / 8000.0) < 1e-9
+    assert abs(p["frac_step"] - p["achieved_gbs_step"] / r["peak"]) < 1e-9
+    assert p["e2e"]["value"] > 0 and p["e2e"]["h2d_bytes_per_step"] > 0
+    assert d["config"] == bench.config_of(make_workload("tiny"))
+    assert d["clocks"]["samples"] >= 1
 
 
 def test_next_rows_lines():

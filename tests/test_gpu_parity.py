@@ -2,8 +2,9 @@
 
 Small and medium cases are compared in full (every metadata entry, every output byte
 including the rows the kernels must leave untouched, every combined element); the
-full-size workloads run in the benchmark's launch configuration and are compared in
-full for the metadata and on a seeded sample of tokens for dispatch and combine.
+full-size workloads run in the benchmark's launch configuration and are compared in full
+too: every metadata entry, every written row and scale row, the sentinel left in every row
+no pair maps to, and every combined element.
 """
 import numpy as np
 import pytest
@@ -12,7 +13,7 @@ import torch
 import oracle
 from workloads import bf16_bits_to_f32, f32_to_bf16_bits, make_case, make_workload, random_bf16
 
-from _harness import (bytes_of, check_combine, gpu_meta, moe, run_full, run_sampled, to_dev)
+from _harness import (bytes_of, check_combine, gpu_meta, moe, run_full, run_full_large, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,15 +49,17 @@ def test_decode_workload_full():
 
 
 @pytest.mark.parametrize("name", ["prefill", "qwen3", "nvfp4"])
-def test_full_size_workloads_sampled(name):
-    run_sampled(make_workload(name))
+def test_full_size_workloads_in_full(name):
+    """prefill (normal FP8, Zipf routing, H=7168), qwen3 (normal bf16, 5 % empty slots) and nvfp4
+    (masked NVFP4, M=8192): every byte and every combined element against the oracle."""
+    run_full_large(make_workload(name))
 
 
 def test_qwen3_masked_secondary():
-    """qwen3 routing in the masked layout with M = T (no capacity drops)."""
+    """qwen3 routing in the masked layout with M = T (no capacity drops), compared in full."""
     w = make_workload("qwen3")
     w.mode, w.M = "masked", w.T
-    run_sampled(w, n_sample=128)
+    run_full_large(w)
 
 
 # --- shapes: ragged slices, several blocks, limits ------------------------------

@@ -89,33 +89,43 @@ def test_partitioned_dispatch_and_combine_match_oracle(T, S, H, E, K, P, quant, 
     check_combine(bytes_of(out).view(np.uint16).reshape(T, H), want)
 
 
-def test_partitioned_nvfp4_workload_layout_and_sampled_rows():
-    """The nvfp4 workload (T=8192, H=7168, E=256, K=8, P=8) through the FlashInfer layout:
-    sanitised ids and weights in full, NVFP4 rows on a sample of tokens."""
+@pytest.mark.parametrize("layout", ["row", "swizzled"])
+def test_partitioned_nvfp4_workload_in_full(layout):
+    """The nvfp4 workload (T=8192, H=7168, E=256, K=8, P=8, one receive slot per token) through
+    the FlashInfer layout, in the benchmark's launch configuration: every receive row, scale,
+    sanitised id and weight (row-major or swizzled scales), the untouched payload of slots a
+    partition does not receive, and every element of the partitioned combine."""
     m = moe()
     w = make_workload("nvfp4")
     x, ids, wt = to_dev(w)
-    P, S, K, H = w.P, w.T, w.K, w.H
-    rx = torch.empty((P, S, H // 2), dtype=torch.uint8, device="cuda")
-    rsf = torch.empty((P, S, H // 16), dtype=torch.uint8, device="cuda")
-    rids = torch.empty((P, S, K), dtype=torch.int32, device="cuda")
-    rw = torch.zeros((P, S, K), dtype=torch.float32, device="cuda")
+    P, S, K, H, E = w.P, w.T, w.K, w.H, w.E
+    rx = filled((P, S, H // 2), torch.uint8)
+    rsf = filled((m.swizzled_scale_bytes(P * S, H),) if layout == "swizzled" else (P, S, H // 16), torch.uint8)
+    rids = filled((P, S, K), torch.int32)
+    rw = filled((P, S, K), torch.float32)
     st = m.new_status()
-    m.moe_dispatch_partitioned("nvfp4b16", x, ids, wt, w.E, P, rx, rsf, rids, rw, st, input_global_scale=w.global_scale)
+    m.moe_dispatch_partitioned_ex("nvfp4b16", layout, x, ids, wt, E, P, rx, rsf, rids, rw, st,
+                                  input_global_scale=w.global_scale)
+    ox, osf, oids, ow = oracle.dispatch_partitioned("nvfp4b16", w.x, w.topk_ids, w.topk_weights, E, P,
+                                                    global_scale=w.global_scale, num_slots=S, fill=SENTINEL)
     torch.cuda.synchronize()
-    gids = rids.cpu().numpy()
-    ep = w.E // P
-    part = np.where(w.topk_ids >= 0, w.topk_ids // ep, -1)
-    for p in range(P):
-        want = np.where(part == p, w.topk_ids, -1)
-        routed = (part == p).any(axis=1)
-        want[~routed] = -1
-        assert np.array_equal(gids[p], want)
-    rng = np.random.default_rng(5)
-    for t in rng.choice(w.T, 64, replace=False):
-        q, sf = oracle.quant_nvfp4_row(w.x[t], w.global_scale)
-        for p in set(part[t][part[t] >= 0].tolist()):
-            assert np.array_equal(rx[p, t].cpu().numpy(), q) and np.array_equal(rsf[p, t].cpu().numpy(), sf)
+    assert int(st.item()) == 0
+    assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
+    if layout == "swizzled":
+        assert np.array_equal(rsf.cpu().numpy(), oracle.nvfp4_sf_interleave(osf.reshape(P * S, H // 16)))
+    else:
+        assert np.array_equal(bytes_of(rsf), osf.reshape(P, -1))
+    assert np.array_equal(rids.cpu().numpy(), oids)
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
+    del rx, rsf, rids, rw, ox, osf
+
+    partial_h = random_bf16(np.random.default_rng(77), (P, S, H))
+    partial = torch.from_numpy(partial_h.view(np.int16)).cuda().view(torch.bfloat16)
+    out = filled((w.T, H), torch.bfloat16)
+    m.moe_combine_partitioned(partial, ids, E, P, out, st)
+    want = oracle.combine_partitioned(partial_h, w.topk_ids, E, P)
+    torch.cuda.synchronize()
+    check_combine(bytes_of(out).view(np.uint16).reshape(w.T, H), want)
     assert int(st.item()) == 0
 
 
