@@ -843,8 +843,9 @@ def run_next_rows(args):
                                                      input_global_scale=g)
         us = timed_us(fn)
         emit("f1", f"moe_dispatch_partitioned_ex({quant}, {layout} scales)", "nvfp4", T, us, nbytes,
-             ["dispatch_partitioned_kernel"] + (["sf_swizzle_pad_kernel"] if layout == "swizzled" else []),
-             2 if layout == "swizzled" else 1)
+             (["sf_tiles_clear_kernel"] if layout == "swizzled" else []) + ["dispatch_bulk_quant_kernel"]
+             + (["sf_tiles_interleave_kernel"] if layout == "swizzled" else []),
+             3 if layout == "swizzled" else 1)
         del rx, rsf, rids, rw
     partial = torch.randn((P, S, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -919,7 +920,7 @@ def run_next_rows(args):
                                      st, M, input_global_scale=w.global_scale)
     emit("f3", "moe_dispatch_ex(nvfp4b16 masked, swizzled 128x4 scales)", "nvfp4", T, timed_us(fn),
          2 * T * H + 8 * T * K + 8 * E + rows * row_bytes("nvfp4b16", H),
-         ["dispatch_kernel", "sf_swizzle_pad_kernel"], 2)
+         ["sf_tiles_clear_kernel", "dispatch_bulk_quant_kernel", "sf_tiles_interleave_kernel"], 3)
     torch.cuda.synchronize()
     moe.check_status(st, "next rows")
 

@@ -112,12 +112,10 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
 
         for (int k0 = 0; k0 < a.K; k0 += kBatch) {
             int64_t rows[kBatch];
-            float wk[kBatch];
 #pragma unroll
             for (int j = 0; j < kBatch; j++) {
                 const int k = k0 + j;
                 rows[j] = __shfl_sync(kFullMask, my_row, k & 31);
-                wk[j] = __shfl_sync(kFullMask, my_w, k & 31);
                 if (k >= a.K || !act0) rows[j] = -1;
             }
             uint4 v[kBatch][2];
@@ -131,6 +129,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(CombineArgs a)
                     if (act1) v[j][1] = ld_stream_v4(p + col1);
                 }
             }
+            // the weights are shuffled only now: the row loads above do not wait for them
+            // (a weight load may still be in flight from memory when the rows are addressed)
+            float wk[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; j++) wk[j] = __shfl_sync(kFullMask, my_w, (k0 + j) & 31);
             // the next unit's slot metadata rides along with this unit's row loads
             if (k0 + kBatch >= a.K) {
                 const int64_t un = u + nwarps;

@@ -66,6 +66,9 @@ struct DispatchArgs {
     const float* w;
     int32_t* recv_ids;
     float* recv_w;
+    // the scale rows are read back by a later kernel of the call (the swizzled layout's
+    // in-place interleave): bulk kernels store them with an L2 evict-last policy
+    bool keep_scales_in_l2;
 };
 
 // destination row of pair t*K + lane (lanes >= K return -1); s_seg: seg_indptr in smem
@@ -324,9 +327,15 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
     }
 }
 
+// How the bulk quantising kernel writes scale rows: one bulk store per row; by its threads
+// (layouts a bulk row store cannot write); or one bulk store per row with an L2 evict-last
+// policy (rows a later kernel of the same call reads back: the swizzled layout's interleave).
+constexpr int kScalesBulk = 0, kScalesThreads = 1, kScalesBulkKeep = 2;
+
 // quantising modes: 256 threads quantise shared -> shared; thread 0 drives the copies
-template <int QUANT, bool MASKED, bool PART, bool TS>
+template <int QUANT, bool MASKED, bool PART, int SCALES>
 __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(DispatchArgs a, BulkGeom geo) {
+    constexpr bool TS = SCALES == kScalesThreads;
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait();
     if constexpr (PART) partition_padding_ids(a);
@@ -410,9 +419,12 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
                 const int64_t row = s_rows[o * kBulkRows + k];
                 if (row < 0) continue;
                 bulk_store(static_cast<uint8_t*>(a.out_q) + row * geo.q_bytes, out0 + o * out_bytes, geo.q_bytes);
-                if (!TS)
+                if constexpr (SCALES == kScalesBulk)
                     bulk_store(static_cast<uint8_t*>(a.out_s) + row * geo.s_bytes, out0 + o * out_bytes + geo.q_bytes,
                                geo.s_bytes);
+                if constexpr (SCALES == kScalesBulkKeep)
+                    bulk_store_hint(static_cast<uint8_t*>(a.out_s) + row * geo.s_bytes,
+                                    out0 + o * out_bytes + geo.q_bytes, geo.s_bytes, l2_policy_evict_last());
             }
             bulk_commit();
         }
@@ -479,8 +491,10 @@ cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkG
         const int grid = int(std::min<int64_t>(a.T, int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1)));
         return launch_pdl(ctx, kern, dim3(grid), dim3(threads), smem, a, geo);
     } else {
-        auto kern = geo.ts ? dispatch_bulk_quant_kernel<QUANT, MASKED, PART, true>
-                           : dispatch_bulk_quant_kernel<QUANT, MASKED, PART, false>;
+        auto kern = geo.ts ? dispatch_bulk_quant_kernel<QUANT, MASKED, PART, kScalesThreads>
+                           : dispatch_bulk_quant_kernel<QUANT, MASKED, PART, kScalesBulk>;
+        if constexpr (QUANT == MOE_QUANT_NVFP4_B16)
+            if (!geo.ts && a.keep_scales_in_l2) kern = dispatch_bulk_quant_kernel<QUANT, MASKED, PART, kScalesBulkKeep>;
         // as many passes over the row's 16-element slices as 256 threads need, with the block
         // sized so that every pass is full (H = 7168: 448 slices = 2 x 224, not 256 + 192)
         const int nslices = a.H / kLaneElems;
@@ -601,32 +615,11 @@ cudaError_t launch_convert_probe(const LaunchCtx& ctx, const float* in, int64_t 
     return cudaGetLastError();
 }
 
-// Zeros of the padding rows [R, roundup(R, 128)) of a 128 x 4 swizzled scale matrix with C
-// columns (C % 4 == 0): one thread per 4-byte word (row, tile column).
-__global__ void sf_swizzle_pad_kernel(uint8_t* sf, int64_t R, int C, int64_t n_words) {
-    pdl_wait();
-    const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (j >= n_words) return;
-    const int C4 = C / 4;
-    const int64_t r = R + j / C4;
-    const int ct = int(j - (j / C4) * C4);
-    *reinterpret_cast<uint32_t*>(sf + swizzled_128x4_index(r, 4 * ct, C)) = 0u;
-}
-
-cudaError_t launch_sf_swizzle_pad(const LaunchCtx& ctx, uint8_t* sf, int64_t R, int C) {
-    const int64_t Rp = (R + 127) / 128 * 128;
-    const int64_t n_words = (Rp - R) * (C / 4);
-    if (n_words == 0) return cudaSuccess;
-    const int threads = 256;
-    return launch_pdl(ctx, sf_swizzle_pad_kernel, dim3(unsigned((n_words + threads - 1) / threads)), dim3(threads),
-                      0, sf, R, C, n_words);
-}
-
 cudaError_t launch_dispatch_partitioned_bulk(const LaunchCtx& ctx, int quant, const uint16_t* x, int64_t T,
                                              int64_t S, int H, const int32_t* ids, const float* w, int K, int E,
                                              int P, int32_t invalid_id, float g, void* recv_x, uint8_t* recv_sf,
                                              int32_t* recv_ids, float* recv_w, int32_t* dev_status,
-                                             int scale_layout, bool* launched) {
+                                             int scale_layout, bool* launched, bool keep_scales_in_l2) {
     *launched = false;
     if (T < kBulkMinTokens || (quant != MOE_QUANT_NONE && quant != MOE_QUANT_NVFP4_B16)) return cudaSuccess;
     DispatchArgs a{};
@@ -651,6 +644,7 @@ cudaError_t launch_dispatch_partitioned_bulk(const LaunchCtx& ctx, int quant, co
     a.w = w;
     a.recv_ids = recv_ids;
     a.recv_w = recv_w;
+    a.keep_scales_in_l2 = keep_scales_in_l2;
     const BulkGeom geo = bulk_geometry(quant, a);
     if (geo.stages == 0) return cudaSuccess;
     *launched = true;
@@ -684,25 +678,52 @@ cudaError_t launch_dispatch(const LaunchCtx& ctx, int mode, int quant, const uin
     a.L.kind = scale_layout;
     a.L.M = masked ? M : 0;
     a.L.rows_al = ((masked ? int64_t(M) : a.max_row) + 3) / 4 * 4;
+    // swizzled NVFP4 scales: when the buffer allows it, the scale rows go out row-major and the
+    // touched tiles are interleaved in place afterwards (the interleave zeroing the rows the
+    // dispatch does not write, or a clear of the touched tiles first where it cannot tell them);
+    // else the touched tiles are cleared and every scale word is stored at its tile position
+    SfTiles tiles{};
+    bool by_tiles = false;
     if (scale_layout == MOE_SCALES_SWIZZLED_128X4) {
-        cudaError_t err = launch_sf_swizzle_pad(ctx, static_cast<uint8_t*>(out_scales),
-                                                masked ? int64_t(E) * M : a.max_row, H / 16);
+        tiles.sf = static_cast<uint8_t*>(out_scales);
+        tiles.R = masked ? int64_t(E) * M : a.max_row;
+        tiles.C = H / 16;
+        tiles.kind = masked ? kSfTilesMasked : kSfTilesAll;
+        tiles.seg = seg_indptr;
+        tiles.E = E;
+        tiles.M = M;
+        tiles.n_blocks = (tiles.R + 127) / 128;
+        // a group's run: a quarter above the mean pairs per expert (longer runs loop), at most M
+        tiles.q_per_group = sf_tiles_q_per_group(std::min<int64_t>(M, (5 * T * K / E + 3) / 4), E);
+        tiles.status = dev_status;
+        by_tiles = sf_tiles_interleavable(tiles);
+        cudaError_t err = sf_tiles_interleave_zeroes(tiles) ? cudaSuccess : launch_sf_tiles_clear(ctx, tiles);
         if (err != cudaSuccess) return err;
+        if (by_tiles) {
+            a.L.kind = MOE_SCALES_ROW_MAJOR;
+            a.keep_scales_in_l2 = true;
+        }
     }
+    cudaError_t err;
     switch (quant) {
         case MOE_QUANT_NONE:
-            return masked ? launch_variant<MOE_QUANT_NONE, true>(ctx, a)
-                          : launch_variant<MOE_QUANT_NONE, false>(ctx, a);
+            err = masked ? launch_variant<MOE_QUANT_NONE, true>(ctx, a) : launch_variant<MOE_QUANT_NONE, false>(ctx, a);
+            break;
         case MOE_QUANT_FP8_G128:
-            return masked ? launch_variant<MOE_QUANT_FP8_G128, true>(ctx, a)
-                          : launch_variant<MOE_QUANT_FP8_G128, false>(ctx, a);
+            err = masked ? launch_variant<MOE_QUANT_FP8_G128, true>(ctx, a)
+                         : launch_variant<MOE_QUANT_FP8_G128, false>(ctx, a);
+            break;
         case MOE_QUANT_FP8_G128_UE8M0:
-            return masked ? launch_variant<MOE_QUANT_FP8_G128_UE8M0, true>(ctx, a)
-                          : launch_variant<MOE_QUANT_FP8_G128_UE8M0, false>(ctx, a);
+            err = masked ? launch_variant<MOE_QUANT_FP8_G128_UE8M0, true>(ctx, a)
+                         : launch_variant<MOE_QUANT_FP8_G128_UE8M0, false>(ctx, a);
+            break;
         default:
-            return masked ? launch_variant<MOE_QUANT_NVFP4_B16, true>(ctx, a)
-                          : launch_variant<MOE_QUANT_NVFP4_B16, false>(ctx, a);
+            err = masked ? launch_variant<MOE_QUANT_NVFP4_B16, true>(ctx, a)
+                         : launch_variant<MOE_QUANT_NVFP4_B16, false>(ctx, a);
+            break;
     }
+    if (err != cudaSuccess || !by_tiles) return err;
+    return launch_sf_tiles_interleave(ctx, tiles);
 }
 
 }  // namespace moe

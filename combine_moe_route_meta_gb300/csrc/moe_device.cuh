@@ -145,7 +145,26 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, uint32_
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src_smem), "r"(bytes)
                  : "memory");
 }
+// the same with an L2 cache policy (createpolicy) for the written lines
+__device__ __forceinline__ void bulk_store_hint(void* dst, uint32_t src_smem, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(src_smem), "r"(bytes), "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// L2 policy that keeps the lines it covers in L2 ahead of normally cached ones: for data that a
+// later kernel of the same call reads back (the row-major scale rows of the swizzled layout).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void st_v4_hint(void* ptr, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w), "l"(policy)
+                 : "memory");
+}
 // wait until at most N of this thread's committed bulk groups still read shared memory
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {

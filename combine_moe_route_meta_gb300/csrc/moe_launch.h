@@ -119,7 +119,7 @@ cudaError_t launch_dispatch_partitioned_bulk(const LaunchCtx& ctx, int quant, co
                                              int64_t S, int H, const int32_t* ids, const float* w, int K, int E,
                                              int P, int32_t invalid_id, float g, void* recv_x, uint8_t* recv_sf,
                                              int32_t* recv_ids, float* recv_w, int32_t* dev_status,
-                                             int scale_layout, bool* launched);
+                                             int scale_layout, bool* launched, bool keep_scales_in_l2 = false);
 
 // moe_dispatch_layout runs as one block (ids staged in shared memory, no memsets, no global
 // atomics) up to this many (token, k) pairs. Measured after an L2 flush: one block 10.2 us
@@ -141,9 +141,38 @@ cudaError_t launch_route_dispatch_small(const LaunchCtx& ctx, int mode, int quan
                                         int32_t* partition_counts, void* out_q, void* out_scales,
                                         int32_t* dev_status);
 
-// Zeros of the padding rows [R, roundup(R, 128)) of a 128 x 4 swizzled NVFP4 scale matrix
-// with C columns (C % 4 == 0; sf 4-byte aligned). dispatch.cu.
-cudaError_t launch_sf_swizzle_pad(const LaunchCtx& ctx, uint8_t* sf, int64_t R, int C);
+// The 128 x 4 swizzled NVFP4 scale layout by whole tiles (sf_swizzle.cu): the touched 128-row
+// blocks of the [R, C] scale matrix (sf 4-byte aligned, C % 4 == 0) are cleared, the dispatch
+// writes its scale rows row-major into the same buffer, and the blocks are then interleaved
+// in place.
+constexpr int kSfTilesAll = 0;          // contiguous layout: every block of [0, roundup(R, 128))
+constexpr int kSfTilesMasked = 1;       // blocks overlapping e*M + [0, min(M, seg[e+1] - seg[e]))
+constexpr int kSfTilesPartitioned = 2;  // blocks overlapping p*S + [0, T)
+struct SfTiles {
+    uint8_t* sf;
+    int64_t R;          // rows of the scale matrix
+    int C;              // columns (bytes per row), C % 4 == 0
+    int kind;
+    const int64_t* seg; // masked: seg_indptr [E+1]
+    int E, M;           // masked
+    int P;              // partitioned
+    int64_t S, T;       // partitioned: slots per partition, tokens
+    int64_t n_blocks;   // roundup(R, 128) / 128
+    int64_t q_per_group;  // CTAs per expert / partition (sf_tiles_q_per_group)
+    int32_t* status;      // MOE_ERR_TIMEOUT if a bounded wait of the interleave gives up
+    const int32_t* ids;   // partitioned: topk_ids [T, K] (which slots a partition receives)
+    int K, ep;            // partitioned: top-k, experts per partition
+};
+// CTAs per group for groups of about `rows_per_group_guess` touched rows.
+int64_t sf_tiles_q_per_group(int64_t rows_per_group_guess, int64_t groups);
+// Whether the blocks can be interleaved in place (sf 16-byte aligned, a 128-row block fits in
+// shared memory); otherwise the dispatch stores each scale word at its tile position.
+bool sf_tiles_interleavable(const SfTiles& a);
+// Whether the interleave itself zeroes the rows of a touched block that the dispatch does not
+// write (masked and partitioned layouts), so that no clear has to run before the dispatch.
+bool sf_tiles_interleave_zeroes(const SfTiles& a);
+cudaError_t launch_sf_tiles_clear(const LaunchCtx& ctx, const SfTiles& a);
+cudaError_t launch_sf_tiles_interleave(const LaunchCtx& ctx, const SfTiles& a);
 
 // Per-partition layout and the FlashInfer all-to-all layout (partitioned.cu).
 constexpr int kMaxPartitionsA2A = 32;

@@ -321,19 +321,47 @@ cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const u
     a.units_per_row = (H + kSlice - 1) / kSlice;
     a.n_units = T * a.units_per_row;
     a.L = ScaleLayout{scale_layout, 0, 0};
+    // swizzled NVFP4 scales: when the buffer allows it, the scale rows go out row-major and the
+    // touched tiles are interleaved in place afterwards (the interleave zeroing the rows the
+    // dispatch does not write, or a clear of the touched tiles first where it cannot tell them);
+    // else the touched tiles are cleared and every scale word is stored at its tile position
+    SfTiles tiles{};
+    bool by_tiles = false;
     if (quant == MOE_QUANT_NVFP4_B16 && scale_layout == MOE_SCALES_SWIZZLED_128X4) {
-        cudaError_t err = launch_sf_swizzle_pad(ctx, recv_sf, int64_t(P) * S, H / 16);
+        tiles.sf = recv_sf;
+        tiles.R = int64_t(P) * S;
+        tiles.C = H / 16;
+        tiles.kind = kSfTilesPartitioned;
+        tiles.P = P;
+        tiles.S = S;
+        tiles.T = T;
+        tiles.n_blocks = (tiles.R + 127) / 128;
+        tiles.q_per_group = sf_tiles_q_per_group(T, P);
+        tiles.status = dev_status;
+        tiles.ids = ids;
+        tiles.K = K;
+        tiles.E = E;
+        tiles.ep = E / P;
+        by_tiles = sf_tiles_interleavable(tiles);
+        cudaError_t err = sf_tiles_interleave_zeroes(tiles) ? cudaSuccess : launch_sf_tiles_clear(ctx, tiles);
         if (err != cudaSuccess) return err;
+        if (by_tiles) {
+            scale_layout = MOE_SCALES_ROW_MAJOR;
+            a.L.kind = MOE_SCALES_ROW_MAJOR;
+        }
     }
     bool bulk = false;
     cudaError_t err = launch_dispatch_partitioned_bulk(ctx, quant, x, T, S, H, ids, w, K, E, P, invalid_id, g,
                                                        recv_x, recv_sf, recv_ids, recv_w, dev_status, scale_layout,
-                                                       &bulk);
-    if (err != cudaSuccess || bulk) return err;
-    const int64_t pad = (S - T) * P * K;
-    if (a.n_units == 0 && pad == 0) return cudaSuccess;
-    if (quant == MOE_QUANT_NVFP4_B16) return launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NVFP4_B16>, a, pad);
-    return launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NONE>, a, pad);
+                                                       &bulk, by_tiles);
+    if (err == cudaSuccess && !bulk) {
+        const int64_t pad = (S - T) * P * K;
+        if (a.n_units > 0 || pad > 0)
+            err = quant == MOE_QUANT_NVFP4_B16 ? launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NVFP4_B16>, a, pad)
+                                               : launch_units(ctx, dispatch_partitioned_kernel<MOE_QUANT_NONE>, a, pad);
+    }
+    if (err != cudaSuccess || !by_tiles) return err;
+    return launch_sf_tiles_interleave(ctx, tiles);
 }
 
 cudaError_t launch_combine_partitioned(const LaunchCtx& ctx, const uint16_t* partial, int64_t T, int64_t S, int H,

@@ -87,8 +87,19 @@ typedef enum {
                                   FlashinferDispatcher.dispatch): scale (r, c) at byte
                                   ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4.
                                   R = out_rows (normal), E*M (masked) or P*num_slots (partitioned);
-                                  the buffer holds roundup(R, 128)*C bytes and the padding rows
-                                  R..roundup(R, 128)-1 are written as zeros. 4-byte aligned.  */
+                                  the buffer holds roundup(R, 128)*C bytes, 4-byte aligned
+                                  (16-byte aligned: the fast path, whole tiles written at once).
+                                  Every 128-row tile the call touches is written in full: its
+                                  destination rows hold their scales, all its other rows (and the
+                                  padding rows R..roundup(R, 128)-1) zeros. Touched tiles: every
+                                  tile (normal); those overlapping rows e*M + [0, min(M,
+                                  seg_indptr[e+1] - seg_indptr[e])) of some expert e (masked);
+                                  those overlapping slots p*num_slots + [0, T) of some partition p
+                                  (partitioned); and the tile holding the padding rows. Other
+                                  tiles keep their previous bytes. Masked layout: seg_indptr must
+                                  come without expert alignment (moe_route_meta, or
+                                  expert_alignment 1); with aligned segments the rows between an
+                                  expert's pair count and its segment length are unspecified.  */
 } moe_scale_layout_t;
 
 #define MOE_MAX_EXPERTS 1024   /* E <= 1024                                  */
@@ -384,9 +395,13 @@ moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t *hidden_
  * scale_layout MOE_SCALES_SWIZZLED_128X4 writes recv_scales already interleaved, as
  * FlashinferDispatcher.dispatch (flashinfer.py page) obtains them by applying
  * nvfp4_block_scale_interleave to the received scales viewed as [P*num_slots, H/16] before the
- * CUTLASS MoE: R = P*num_slots rows, roundup(R, 128)*H/16 bytes, padding rows zero; slots a
- * partition does not receive are left untouched as in the row-major layout. NVFP4 only,
- * H % 64 == 0, recv_scales 4-byte aligned. MOE_SCALES_ROW_MAJOR is moe_dispatch_partitioned.
+ * CUTLASS MoE: R = P*num_slots rows, roundup(R, 128)*H/16 bytes. The tiles holding slots
+ * t < T of some partition, and the one holding the padding rows, are written in full: slots a
+ * partition does not receive are zero there, like the padding rows (moe_scale_layout_t); tiles
+ * of padding slots only keep their bytes. NVFP4 only, H % 64 == 0, recv_scales 4-byte aligned.
+ * Launches: a clear of the touched tiles, the dispatch, and (recv_scales 16-byte aligned) an
+ * in-place interleave of the row-major scale rows the dispatch wrote there.
+ * MOE_SCALES_ROW_MAJOR is moe_dispatch_partitioned.
  * Everything else as moe_dispatch_partitioned.
  */
 moe_status_t moe_dispatch_partitioned_ex(moe_quant_t quant, moe_scale_layout_t scale_layout,

@@ -158,6 +158,55 @@ def run_full(w: Workload, *, expert_seed: int = 1234, check_untouched: bool = Tr
     return om
 
 
+def swizzled_scales_expected(osf: np.ndarray, written: np.ndarray, touched_rows: np.ndarray) -> np.ndarray:
+    """The expected swizzled NVFP4 scale buffer: the oracle's row-major scales osf [R, C] (rows no
+    pair maps to hold the fill) with every unwritten row of a touched 128-row block set to zero,
+    through the oracle's interleave (which zero-pads to a multiple of 128 rows).
+
+    written:      bool [R], the rows a pair maps to.
+    touched_rows: bool [R], the rows that decide which blocks the call touches (the block holding
+                  the padding rows, if any, is touched as well)."""
+    R = osf.shape[0]
+    nb = (R + 127) // 128
+    blk = np.zeros(nb, bool)
+    idx = np.nonzero(touched_rows)[0]
+    blk[idx // 128] = True
+    if R % 128:
+        blk[-1] = True
+    in_touched = np.repeat(blk, 128)[:R]
+    out = osf.copy()
+    out[in_touched & ~written] = 0
+    return oracle.nvfp4_sf_interleave(out)
+
+
+def masked_touched_rows(seg: np.ndarray, E: int, M: int) -> np.ndarray:
+    """Rows e*M + [0, min(M, seg[e+1] - seg[e])) of the masked layout [E*M]."""
+    rows = np.zeros(E * M, bool)
+    for e in range(E):
+        n = min(M, int(seg[e + 1] - seg[e]))
+        rows[e * M:e * M + n] = True
+    return rows
+
+
+def partitioned_routed(topk_ids: np.ndarray, E: int, P: int, S: int) -> np.ndarray:
+    """bool [P*S]: slot t of partition p receives token t (some valid id of t lies in p)."""
+    T, K = topk_ids.shape
+    ep = E // P
+    routed = np.zeros((P, S), bool)
+    for k in range(K):
+        e = topk_ids[:, k]
+        ok = (e >= 0) & (e < E)
+        routed[e[ok] // ep, np.nonzero(ok)[0]] = True
+    return routed.reshape(-1)
+
+
+def partitioned_touched_rows(P: int, S: int, T: int) -> np.ndarray:
+    """Slots [0, T) of every partition's S receive slots."""
+    rows = np.zeros((P, S), bool)
+    rows[:, :T] = True
+    return rows.reshape(-1)
+
+
 def _sentinel_buffer(shape, dtype) -> torch.Tensor:
     """A device buffer of `shape` whose every byte is SENTINEL."""
     n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()

@@ -9,7 +9,8 @@ import torch
 import oracle
 from workloads import make_case, random_bf16
 
-from _harness import SENTINEL, bytes_of, check_combine, filled, moe, to_dev
+from _harness import (SENTINEL, bytes_of, check_combine, filled, masked_rows, masked_touched_rows, moe, to_dev,
+                      swizzled_scales_expected)
 
 pytestmark = pytest.mark.gpu
 
@@ -260,6 +261,17 @@ def test_ue8m0_bulk_path_normal_layout():
 
 # --- NVFP4 block scales in the 128 x 4 swizzled layout (nvfp4_block_scale_interleave) --------
 
+@pytest.mark.parametrize("mode,T,H,E,K,M,offset", [
+    ("normal", 300, 1024, 24, 6, 0, 4),      # scale buffer 4-byte aligned only: words stored in place
+    ("masked", 1100, 7168, 64, 8, 200, 4),
+    ("masked", 96, 1024, 16, 4, 30, 12),
+])
+def test_nvfp4_swizzled_scales_unaligned_buffer(mode, T, H, E, K, M, offset):
+    """A swizzled scale buffer that is 4- but not 16-byte aligned gets the same bytes (its tiles
+    cleared, then every scale word stored at its tile position) as an aligned one."""
+    _swizzled_case(mode, T, H, E, K, M, offset)
+
+
 @pytest.mark.parametrize("mode,T,H,E,K,M", [
     ("normal", 300, 1024, 24, 6, 0),     # 1800 rows -> padded to 1920
     ("normal", 1500, 2048, 64, 8, 0),    # >= 1024 tokens: the bulk kernel, its threads storing the scales
@@ -270,8 +282,13 @@ def test_ue8m0_bulk_path_normal_layout():
     ("masked", 1100, 1088, 64, 8, 200),  # H % 256 != 0: the bulk kernel still stores the swizzled words
 ])
 def test_nvfp4_swizzled_scales_match_oracle_interleave(mode, T, H, E, K, M):
-    """The whole scale buffer equals the oracle's row-major scales (untouched rows keep
-    their fill) passed through the interleave: padding rows zero, codes unchanged."""
+    """The whole scale buffer equals the oracle's row-major scales passed through the interleave,
+    where every 128-row block the call touches is written in full (rows no pair maps to are zero,
+    and so are the padding rows) and every other block keeps its fill; codes unchanged."""
+    _swizzled_case(mode, T, H, E, K, M, 0)
+
+
+def _swizzled_case(mode, T, H, E, K, M, offset):
     m = moe()
     w = make_case(T, H, E, K, seed=T + H, mode=mode, quant="nvfp4b16", M=M, invalid_rate=0.05)
     x, ids, _ = to_dev(w)
@@ -280,13 +297,18 @@ def test_nvfp4_swizzled_scales_match_oracle_interleave(mode, T, H, E, K, M):
     s2d = torch.from_numpy(om.src2dst).cuda()
     R = T * K if mode == "normal" else E * M
     q = filled((R, H // 2), torch.uint8)
-    sf = filled((m.swizzled_scale_bytes(R, H),), torch.uint8)
+    nsf = m.swizzled_scale_bytes(R, H)
+    sf = filled((nsf + 16,), torch.uint8)[offset:offset + nsf]
     st = m.new_status()
     m.moe_dispatch_ex(mode, "nvfp4b16", "swizzled", x, ids, E, s2d, seg, q, sf, st, max_tokens_per_expert=M,
                       input_global_scale=w.global_scale)
     oq, osf = oracle.dispatch(mode, "nvfp4b16", w.x, w.topk_ids, om, E, M=M, global_scale=w.global_scale,
                               rows=R if mode == "normal" else None, fill=SENTINEL)
-    want_sf = oracle.nvfp4_sf_interleave(osf.reshape(R, H // 16))
+    written = np.zeros(R, bool)
+    rows = om.src2dst[om.src2dst >= 0] if mode == "normal" else masked_rows(w, om)
+    written[rows[rows >= 0]] = True
+    touched = np.ones(R, bool) if mode == "normal" else masked_touched_rows(om.seg_indptr, E, M)
+    want_sf = swizzled_scales_expected(osf.reshape(R, H // 16), written, touched)
     torch.cuda.synchronize()
     assert np.array_equal(bytes_of(q).reshape(-1), oq.reshape(-1))
     assert np.array_equal(sf.cpu().numpy(), want_sf)

@@ -12,7 +12,8 @@ import torch
 import oracle
 from workloads import make_case, make_workload, random_bf16
 
-from _harness import SENTINEL, bytes_of, check_combine, filled, moe, to_dev
+from _harness import (SENTINEL, bytes_of, check_combine, filled, moe, partitioned_routed, partitioned_touched_rows,
+                      swizzled_scales_expected, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -112,7 +113,9 @@ def test_partitioned_nvfp4_workload_in_full(layout):
     assert int(st.item()) == 0
     assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
     if layout == "swizzled":
-        assert np.array_equal(rsf.cpu().numpy(), oracle.nvfp4_sf_interleave(osf.reshape(P * S, H // 16)))
+        want = swizzled_scales_expected(osf.reshape(P * S, H // 16), partitioned_routed(w.topk_ids, E, P, S),
+                                        partitioned_touched_rows(P, S, w.T))
+        assert np.array_equal(rsf.cpu().numpy(), want)
     else:
         assert np.array_equal(bytes_of(rsf), osf.reshape(P, -1))
     assert np.array_equal(rids.cpu().numpy(), oids)
@@ -138,8 +141,10 @@ def test_partitioned_nvfp4_workload_in_full(layout):
 ])
 def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
     """moe_dispatch_partitioned_ex with swizzled scales equals the row-major receive scales
-    [P*S, H/16] passed through nvfp4_block_scale_interleave (untouched slots keep their
-    fill, padding rows zero); codes, ids and weights as in the row-major layout."""
+    [P*S, H/16] passed through nvfp4_block_scale_interleave, where every 128-row block holding a
+    slot t < T (or a padding row) is written in full: slots a partition does not receive are
+    zero there, padding rows zero, other blocks keep their fill; codes, ids and weights as in
+    the row-major layout."""
     m = moe()
     w = make_case(T, H, E, K, seed=T * 5 + P, quant="nvfp4b16", invalid_rate=0.05)
     x, ids, wt = to_dev(w)
@@ -154,7 +159,9 @@ def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
                                                     global_scale=w.global_scale, num_slots=S, fill=SENTINEL)
     torch.cuda.synchronize()
     assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
-    assert np.array_equal(rsf.cpu().numpy(), oracle.nvfp4_sf_interleave(osf.reshape(P * S, H // 16)))
+    want = swizzled_scales_expected(osf.reshape(P * S, H // 16), partitioned_routed(w.topk_ids, E, P, S),
+                                    partitioned_touched_rows(P, S, T))
+    assert np.array_equal(rsf.cpu().numpy(), want)
     assert np.array_equal(rids.cpu().numpy(), oids)
     assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
     assert int(st.item()) == 0

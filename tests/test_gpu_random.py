@@ -14,7 +14,8 @@ import torch
 import oracle
 from workloads import make_case
 
-from _harness import SENTINEL, bytes_of, check_meta, filled, moe, run_full, to_dev
+from _harness import (SENTINEL, bytes_of, check_meta, filled, moe, partitioned_routed, partitioned_touched_rows,
+                      run_full, swizzled_scales_expected, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -113,7 +114,9 @@ def test_random_partitioned_layouts(seed):
     torch.cuda.synchronize()
     assert np.array_equal(bytes_of(rx).reshape(-1), np.ascontiguousarray(ox).view(np.uint8).reshape(-1))
     if rsf is not None:
-        want = oracle.nvfp4_sf_interleave(osf.reshape(P * S, H // 16)) if layout == "swizzled" else osf.reshape(-1)
+        want = (swizzled_scales_expected(osf.reshape(P * S, H // 16), partitioned_routed(w.topk_ids, E, P, S),
+                                         partitioned_touched_rows(P, S, T))
+                if layout == "swizzled" else osf.reshape(-1))
         assert np.array_equal(rsf.cpu().numpy().reshape(-1), want.reshape(-1))
     assert np.array_equal(rids.cpu().numpy(), oids)
     assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
