@@ -193,6 +193,52 @@ __device__ __forceinline__ int64_t bulk_dest_row(const DispatchArgs& a, const in
     }
 }
 
+// Token metadata of the partition layout staged in shared memory by warp 0 of the quantising
+// bulk kernel, so that the receive ids and weights of the token's P rows are written after the
+// block barrier by P*K threads at once, not by warp 0 in a loop on the token's critical path.
+struct PartStage {
+    int id[16];      // the token's K expert ids
+    float w[16];     // and weights
+    unsigned routed;  // bit p: partition p receives the token
+    int pad;
+};
+
+// Warp-collective (warp 0): lane p's destination row for token t (p*S + t when partition p owns
+// one of the token's experts, else -1); stages ids, weights and the routed mask in `ps`.
+__device__ __forceinline__ int64_t partition_row_staged(const DispatchArgs& a, int64_t t, int lane, int my_id,
+                                                        float my_w, PartStage* ps) {
+    const bool valid = my_id >= 0 && my_id < a.E;
+    if (!valid && my_id != -1 && lane < a.K) set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
+    bool routed = false;
+    for (int k = 0; k < a.K; k++) {
+        const int e = __shfl_sync(kFullMask, my_id, k);
+        routed |= e >= 0 && e < a.E && e / a.ep == lane;
+    }
+    routed = routed && lane < a.P;
+    const unsigned mask = __ballot_sync(kFullMask, routed);
+    if (lane < a.K) {
+        ps->id[lane] = my_id;
+        ps->w[lane] = my_w;
+    }
+    if (lane == 0) ps->routed = mask;
+    return routed ? int64_t(lane) * a.S + t : -1;
+}
+
+// The receive ids (ids the partition does not own -> invalid_id) and weights (routed
+// partitions only) of token t's P rows, from the staged metadata: entry j < P*K (slot
+// k = j % K of partition p = j / K) by thread j % nthreads.
+__device__ __forceinline__ void partition_meta_store(const DispatchArgs& a, int64_t t, const PartStage* ps, int tid,
+                                                     int nthreads) {
+    for (int j = tid; j < a.P * a.K; j += nthreads) {
+        const int p = j / a.K, k = j - p * a.K;
+        const int id = ps->id[k];
+        const bool rp = (ps->routed >> p) & 1u;
+        const int64_t r = (int64_t(p) * a.S + t) * a.K + k;
+        a.recv_ids[r] = (rp && id >= 0 && id < a.E && id / a.ep == p) ? id : a.invalid_id;
+        if (rp) a.recv_w[r] = ps->w[k];
+    }
+}
+
 // Partition layout: the receive ids of the padding slots t in [T, S) of every partition are
 // invalid_id (grid-stride over all threads of the grid).
 __device__ __forceinline__ void partition_padding_ids(const DispatchArgs& a) {
@@ -216,7 +262,11 @@ struct BulkGeom {
 
 constexpr int kBulkCopyThreads = 32;
 constexpr int kBulkQuantThreads = 256;
-constexpr uint32_t kBulkHeader = 768;  // mbarriers (8 B each) at 0, destination rows (2 x 32 x 8 B) at 256
+// shared-memory header of the bulk kernels: mbarriers (8 B each) at 0, destination rows
+// (2 x 32 x 8 B) at 256, and for the partition layout the staged token metadata at 768
+// (PartStage, 2 x 136 B)
+constexpr uint32_t kBulkHeader = 1152;
+constexpr uint32_t kPartStageOff = 768;
 constexpr int kBulkRows = 32;          // destination rows per token: K <= 16 pairs, or P <= 32 partitions
 
 template <bool MASKED>
@@ -343,6 +393,7 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
     const int NS = geo.stages, H = a.H, nd = PART ? a.P : a.K;
     const uint32_t bar0 = smem_addr(smem);
     int64_t* s_rows = reinterpret_cast<int64_t*>(smem + 256);  // [2][kBulkRows]
+    PartStage* s_part = reinterpret_cast<PartStage*>(smem + kPartStageOff);  // [2], PART only
     unsigned char* in_base = smem + geo.in_off;
     unsigned char* out_base = smem + geo.out_off;                // [2][q_bytes + s_bytes]
     int* s_seg = reinterpret_cast<int*>(out_base + 2 * (geo.q_bytes + geo.s_bytes));
@@ -371,7 +422,14 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
         const int64_t t = blockIdx.x + i * G;
         const int s = int(i % NS), o = int(i & 1);
         if (warp == 0) {
-            const int64_t r = bulk_dest_row<MASKED, PART>(a, s_seg, t, lane, pm, t + G);
+            int64_t r;
+            if constexpr (PART) {
+                const PartMeta cur = pm;
+                if (t + G < a.T) pm.load(a, t + G, lane);
+                r = partition_row_staged(a, t, lane, cur.id, cur.w, s_part + o);
+            } else {
+                r = bulk_dest_row<MASKED, PART>(a, s_seg, t, lane, pm, t + G);
+            }
             if (lane < nd) s_rows[o * kBulkRows + lane] = r;
         }
         if (tid == 0) {
@@ -384,6 +442,7 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
             break;
         }
         consumed = i + 1;
+        if constexpr (PART) partition_meta_store(a, t, s_part + o, tid, nthreads);
         const unsigned char* src = in_base + size_t(s) * geo.in_bytes;
         unsigned char* qo = out_base + size_t(o) * out_bytes;
         unsigned char* so = qo + geo.q_bytes;
