@@ -812,9 +812,27 @@ def run_next_rows(args):
         return x, torch.from_numpy(w.topk_ids).to(dev), torch.from_numpy(w.topk_weights).to(dev)
 
     st = moe.new_status(dev)
+    only = {g for g in args.only.split(",") if g}
+    want = lambda g: not only or g in only
 
     # f1: FlashInfer one-row-per-partition layout (the NVFP4 workload's tokens, 8 partitions,
     # one receive slot per token)
+    if want("f1"):
+        next_rows_f1(args, dev, st, timed_us, emit, dev_in)
+    if want("f2"):
+        next_rows_f2(dev, st, timed_us, emit)
+    if want("f3f4"):
+        next_rows_f3f4(dev, st, timed_us, emit, dev_in)
+    if want("f3-swizzled"):
+        next_rows_f3_swizzled(args, dev, st, timed_us, emit, dev_in)
+    torch.cuda.synchronize()
+    moe.check_status(st, "next rows")
+
+
+def next_rows_f1(args, dev, st, timed_us, emit, dev_in):
+    import torch
+    import combine_moe_route_meta_gb300 as moe
+    from workloads import make_workload
     w = make_workload("nvfp4", seed=0)
     x, ids, wt = dev_in(w)
     T, H, K, E, P = w.T, w.H, w.K, w.E, w.P
@@ -843,9 +861,8 @@ def run_next_rows(args):
                                                      input_global_scale=g)
         us = timed_us(fn)
         emit("f1", f"moe_dispatch_partitioned_ex({quant}, {layout} scales)", "nvfp4", T, us, nbytes,
-             (["sf_tiles_clear_kernel"] if layout == "swizzled" else []) + ["dispatch_bulk_quant_kernel"]
-             + (["sf_tiles_interleave_kernel"] if layout == "swizzled" else []),
-             3 if layout == "swizzled" else 1)
+             ["dispatch_bulk_quant_kernel"] + (["sf_tiles_interleave_kernel"] if layout == "swizzled" else []),
+             2 if layout == "swizzled" else 1)
         del rx, rsf, rids, rw
     partial = torch.randn((P, S, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
@@ -854,6 +871,11 @@ def run_next_rows(args):
          ["combine_partitioned_kernel"], 1)
     del partial, out
 
+
+def next_rows_f2(dev, st, timed_us, emit):
+    import torch
+    import combine_moe_route_meta_gb300 as moe
+    from workloads import make_workload
     # f2: get_dispatch_layout outputs (decode and prefill routing, 8 partitions)
     for name in ("decode", "prefill"):
         w2 = make_workload(name, seed=0)
@@ -866,6 +888,11 @@ def run_next_rows(args):
         emit("f2", "moe_dispatch_layout", name, w2.T, us, 4 * w2.T * w2.K + w2.T * P2 + 4 * P2 + 4 * w2.E,
              ["dispatch_layout_kernel"], 1)
 
+
+def next_rows_f3f4(dev, st, timed_us, emit, dev_in):
+    import torch
+    import combine_moe_route_meta_gb300 as moe
+    from workloads import make_workload
     # f3 / f4 on the prefill workload: expert-aligned metadata from int64 ids, then the FP8
     # dispatch with UE8M0 column-major scales into the aligned segments; FP8 pass-through rows
     w = make_workload("prefill", seed=0)
@@ -905,10 +932,15 @@ def run_next_rows(args):
          ["dispatch_bulk_copy_kernel"], 1)
     del q, sc, codes
 
+
+def next_rows_f3_swizzled(args, dev, st, timed_us, emit, dev_in):
+    import torch
+    import combine_moe_route_meta_gb300 as moe
+    from workloads import make_workload
     # f3: NVFP4 masked dispatch with block scales written in the 128 x 4 swizzled layout
     w = make_workload("nvfp4", seed=0)
     x, ids, wt = dev_in(w)
-    T, H, K, E, M = w.T, w.H, w.K, w.E, w.M
+    T, H, K, E, M = w.T, w.H, w.K, w.E, (args.masked_capacity or w.M)
     d = moe.MoEDispatcher(T, H, K, E, mode="masked", quant="nvfp4b16", num_partitions=w.P,
                           max_tokens_per_expert=M, device=dev)
     d.route(ids)
@@ -918,11 +950,10 @@ def run_next_rows(args):
     sfm = torch.empty((moe.swizzled_scale_bytes(E * M, H),), dtype=torch.uint8, device=dev)
     fn = lambda: moe.moe_dispatch_ex("masked", "nvfp4b16", "swizzled", x, ids, E, d.src2dst, d.seg_indptr, qm, sfm,
                                      st, M, input_global_scale=w.global_scale)
-    emit("f3", "moe_dispatch_ex(nvfp4b16 masked, swizzled 128x4 scales)", "nvfp4", T, timed_us(fn),
+    emit("f3", "moe_dispatch_ex(nvfp4b16 masked, swizzled 128x4 scales)",
+         "nvfp4" if M == w.M else f"nvfp4 (M={M})", T, timed_us(fn),
          2 * T * H + 8 * T * K + 8 * E + rows * row_bytes("nvfp4b16", H),
-         ["sf_tiles_clear_kernel", "dispatch_bulk_quant_kernel", "sf_tiles_interleave_kernel"], 3)
-    torch.cuda.synchronize()
-    moe.check_status(st, "next rows")
+         ["dispatch_bulk_quant_kernel", "sf_tiles_interleave_kernel"], 2)
 
 
 WORKLOAD_NAMES = ("tiny", "decode", "prefill", "qwen3", "nvfp4")
@@ -960,6 +991,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--next-rows", action="store_true",
                     help="instead of the step: time each NEXT-row call (one JSON line per call)")
+    ap.add_argument("--only", default="",
+                    help="--next-rows: comma list of groups to run (f1, f2, f3f4, f3-swizzled); default all")
+    ap.add_argument("--masked-capacity", type=int, default=0,
+                    help="--next-rows: slots per expert M of the masked NVFP4 row (default: the workload's "
+                         "8192; a smaller M moves the same rows with smaller buffers, e.g. for a profiler)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

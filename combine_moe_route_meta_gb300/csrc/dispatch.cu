@@ -263,9 +263,10 @@ struct BulkGeom {
 constexpr int kBulkCopyThreads = 32;
 constexpr int kBulkQuantThreads = 256;
 // shared-memory header of the bulk kernels: mbarriers (8 B each) at 0, destination rows
-// (2 x 32 x 8 B) at 256, and for the partition layout the staged token metadata at 768
+// (2 x 32 x 8 B) at 256; the partition layout adds the staged token metadata at 768
 // (PartStage, 2 x 136 B)
-constexpr uint32_t kBulkHeader = 1152;
+constexpr uint32_t kBulkHeader = 768;
+constexpr uint32_t kBulkHeaderPart = 1152;
 constexpr uint32_t kPartStageOff = 768;
 constexpr int kBulkRows = 32;          // destination rows per token: K <= 16 pairs, or P <= 32 partitions
 
@@ -383,8 +384,11 @@ __global__ void __launch_bounds__(kBulkCopyThreads) dispatch_bulk_copy_kernel(Di
 constexpr int kScalesBulk = 0, kScalesThreads = 1, kScalesBulkKeep = 2;
 
 // quantising modes: 256 threads quantise shared -> shared; thread 0 drives the copies
+// The partition layout's variants are held to five CTAs per SM (48 registers with 224-thread
+// blocks: 59.4 against 60.3 us for the NVFP4 workload at 64 registers and four CTAs); the others
+// keep the compiler's choice (a minimum of one block per SM measured 2 us slower there).
 template <int QUANT, bool MASKED, bool PART, int SCALES>
-__global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(DispatchArgs a, BulkGeom geo) {
+__global__ void __launch_bounds__(kBulkQuantThreads, PART ? 5 : 0) dispatch_bulk_quant_kernel(DispatchArgs a, BulkGeom geo) {
     constexpr bool TS = SCALES == kScalesThreads;
     extern __shared__ __align__(128) unsigned char smem[];
     pdl_wait();
@@ -498,7 +502,7 @@ __global__ void __launch_bounds__(kBulkQuantThreads) dispatch_bulk_quant_kernel(
 
 // Row geometry of the bulk path, or stages = 0 when it does not apply (rows or scale rows
 // that are not 16-byte multiples, unaligned bases, column-major scales, shared memory).
-BulkGeom bulk_geometry(int quant, const DispatchArgs& a) {
+BulkGeom bulk_geometry(int quant, const DispatchArgs& a, bool part) {
     BulkGeom g{};
     const int H = a.H;
     g.in_bytes = uint32_t(2 * H);
@@ -518,12 +522,13 @@ BulkGeom bulk_geometry(int quant, const DispatchArgs& a) {
     if (g.q_bytes % 16) return g;
     if (ts) g.s_bytes = (g.s_bytes + 15) / 16 * 16;
     g.ts = ts;
-    const uint32_t seg_bytes = uint32_t(sizeof(int)) * uint32_t(a.E);
+    const bool masked = a.M > 0;  // the masked layout stages seg_indptr after the stages
+    const uint32_t seg_bytes = masked ? uint32_t(sizeof(int)) * uint32_t(a.E) : 0u;
     // ring depth, measured on GB300 (prefill / qwen3 / nvfp4 shapes): the copy mode is flat
     // from 2 to 6 stages; FP8 is best at 3; NVFP4 is best at 2, where its smaller footprint
     // lets 5 CTAs share an SM (61.8 us against 67.7 us at 3 stages for 8192 x 7168)
     const int stages = quant == MOE_QUANT_NONE ? 4 : (quant == MOE_QUANT_NVFP4_B16 ? 2 : 3);
-    g.in_off = kBulkHeader;
+    g.in_off = part ? kBulkHeaderPart : kBulkHeader;
     g.out_off = g.in_off + uint32_t(stages) * g.in_bytes;
     const size_t smem = size_t(g.out_off) + (quant == MOE_QUANT_NONE ? 0 : 2 * (g.q_bytes + g.s_bytes)) + seg_bytes;
     if (smem > 200 * 1024) return g;
@@ -531,13 +536,14 @@ BulkGeom bulk_geometry(int quant, const DispatchArgs& a) {
     return g;
 }
 
-size_t bulk_smem(int quant, const BulkGeom& g, int E) {
-    return size_t(g.out_off) + (quant == MOE_QUANT_NONE ? 0 : 2 * (g.q_bytes + g.s_bytes)) + sizeof(int) * size_t(E);
+size_t bulk_smem(int quant, const BulkGeom& g, int E, bool masked) {
+    return size_t(g.out_off) + (quant == MOE_QUANT_NONE ? 0 : 2 * (g.q_bytes + g.s_bytes)) +
+           (masked ? sizeof(int) * size_t(E) : 0);
 }
 
 template <int QUANT, bool MASKED, bool PART = false>
 cudaError_t launch_bulk(const LaunchCtx& ctx, const DispatchArgs& a, const BulkGeom& geo) {
-    const size_t smem = bulk_smem(QUANT, geo, a.E);
+    const size_t smem = bulk_smem(QUANT, geo, a.E, MASKED);
     int threads;
     int per_sm = 0;
     cudaError_t err;
@@ -571,7 +577,7 @@ template <int QUANT, bool MASKED>
 cudaError_t launch_variant(const LaunchCtx& ctx, const DispatchArgs& a) {
     // large batches: the bulk path when its geometry applies
     if (a.T >= kBulkMinTokens) {
-        const BulkGeom geo = bulk_geometry(QUANT, a);
+        const BulkGeom geo = bulk_geometry(QUANT, a, false);
         if (geo.stages > 0) return launch_bulk<QUANT, MASKED>(ctx, a, geo);
     }
     auto kern = dispatch_kernel<QUANT, MASKED>;
@@ -704,7 +710,7 @@ cudaError_t launch_dispatch_partitioned_bulk(const LaunchCtx& ctx, int quant, co
     a.recv_ids = recv_ids;
     a.recv_w = recv_w;
     a.keep_scales_in_l2 = keep_scales_in_l2;
-    const BulkGeom geo = bulk_geometry(quant, a);
+    const BulkGeom geo = bulk_geometry(quant, a, true);
     if (geo.stages == 0) return cudaSuccess;
     *launched = true;
     return quant == MOE_QUANT_NVFP4_B16 ? launch_bulk<MOE_QUANT_NVFP4_B16, false, true>(ctx, a, geo)
