@@ -277,9 +277,9 @@ __device__ __forceinline__ void stage_seg(const DispatchArgs& a, int* s_seg) {
 }
 
 // TS kernels: the staged scale row `so` of the current token, written by all threads to each
-// destination row in rows[0..nd) (< 0: none) in the output's scale layout. Swizzled NVFP4:
-// 4 consecutive columns of a row are 4 contiguous bytes of the 128 x 4 tile layout, so each
-// row takes H/64 word stores. FP8 fp32 scales: one word per group (column-major, or a
+// destination row in rows[0..nd) (< 0: none) in the output's scale layout. Swizzled NVFP4 (a
+// buffer the in-place interleave cannot take, its tiles cleared first): 4 consecutive columns
+// of a row are 4 contiguous bytes of the 128 x 4 tile layout, so each row takes H/64 word stores. FP8 fp32 scales: one word per group (column-major, or a
 // row-major array whose rows are not 16-byte multiples). UE8M0 and row-major NVFP4 scales:
 // one byte per group, at the index the register path writes.
 template <int QUANT>

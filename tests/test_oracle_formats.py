@@ -131,3 +131,37 @@ def test_sf_interleave_is_a_permutation_of_full_tiles():
     hi = oracle.nvfp4_sf_interleave((idx >> 8).astype(np.uint8))
     where = lo.astype(np.int64) | (hi.astype(np.int64) << 8)
     assert np.array_equal(np.sort(where), np.arange(rows * cols))
+
+
+def test_swizzled_expectation_helper_matches_a_direct_construction():
+    """The test-side expectation of the swizzled scale buffer (tests/_harness.py) equals a direct,
+    element-by-element construction from the layout's definition: scale (r, c) at byte
+    ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4; the rows of a touched 128-row
+    block that no pair maps to, and the padding rows, are zero; other blocks keep the fill."""
+    from _harness import swizzled_scales_expected
+    rng = np.random.default_rng(3)
+    for R, C in ((300, 8), (128, 4), (513, 12)):
+        fill = 0xA5
+        osf = np.full((R, C), fill, np.uint8)
+        written = rng.random(R) < 0.6
+        osf[written] = rng.integers(0, 0x7F, size=(int(written.sum()), C), dtype=np.uint8)
+        touched = np.zeros(R, bool)
+        touched[rng.integers(0, R, size=3)] = True
+        got = swizzled_scales_expected(osf, written, touched)
+        Rp = (R + 127) // 128 * 128
+        want = np.full(Rp * C, fill, np.uint8)
+        blk_touched = np.zeros(Rp // 128, bool)
+        blk_touched[np.nonzero(touched)[0] // 128] = True
+        if R % 128:
+            blk_touched[-1] = True
+        for r in range(Rp):
+            for c in range(C):
+                off = ((r // 128) * (C // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+                if r >= R:
+                    v = 0
+                elif blk_touched[r // 128] and not written[r]:
+                    v = 0
+                else:
+                    v = osf[r, c]
+                want[off] = v
+        assert np.array_equal(got, want)
