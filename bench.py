@@ -868,7 +868,7 @@ def next_rows_f1(args, dev, st, timed_us, emit, dev_in):
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     us = timed_us(lambda: moe.moe_combine_partitioned(partial, ids, E, P, out, st))
     emit("f1", "moe_combine_partitioned", "nvfp4", T, us, routed * 2 * H + 4 * T * K + 2 * T * H,
-         ["combine_partitioned_kernel"], 1)
+         ["combine_partitioned_ring_kernel"], 1)
     del partial, out
 
 

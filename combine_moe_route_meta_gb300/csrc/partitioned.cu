@@ -260,6 +260,136 @@ __global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs 
     }
 }
 
+// The combine for large batches: a ring of whole partial rows in shared memory. One producer warp
+// walks the CTA's tokens and, for each partition the token was sent to (ascending p), bulk-copies
+// the partial row p*S + t into the next ring slot (mbarrier "full" per slot, transaction bytes);
+// eight consumer warps add each token's rows slot by slot (fp32, ascending p, as the register
+// kernel), release every slot on its "empty" mbarrier (one arrival per consumer warp) and write
+// the token's bf16 row. The register kernel keeps at most 8 row slices of 1 KB in flight per warp
+// and uses only the routed ones (about 5.25 of 8 in the nvfp4 workload); the rings hold routed
+// rows only, several small rings per SM. All waits are bounded; a CTA gives up with MOE_ERR_TIMEOUT.
+constexpr int kRingConsumerWarps = 8;
+constexpr int kRingThreads = (kRingConsumerWarps + 1) * 32;
+constexpr int kRingMaxVecs = 4;  // 8-column vectors per consumer thread: H <= 8 * 4 * 256
+constexpr int kRingMaxSlots = 16;
+constexpr int kRingMinSlots = 2;
+constexpr int64_t kRingMinTokens = 1024;
+// Ring size: about 28 KB (two 14 KB rows at H = 7168). Measured on the nvfp4 tokens (P = 8): one
+// 200 KB ring per SM 141.3 us, 100 KB 137.2, 70 KB 131.1, 44 KB 129.0, 28 KB (seven CTAs per SM)
+// 127.0 us; four consumer warps instead of eight 128.0-129.0; a single slot 147.4 us.
+constexpr size_t kRingTargetBytes = 28 * 1024;
+
+// Partitions of the CTA's tokens i0 + lane (stride G from blockIdx.x), one token per lane, as bit
+// masks: every lane loads its token's K ids at once, so a warp pays one round trip for 32 tokens.
+__device__ __forceinline__ unsigned lane_token_partitions(const PartArgs& a, int64_t i0, int64_t ntok, int lane) {
+    const int64_t i = i0 + lane;
+    if (i >= ntok) return 0;
+    const int64_t t = blockIdx.x + i * gridDim.x;
+    int id[MOE_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; k++) id[k] = k < a.K ? __ldg(a.ids + t * a.K + k) : -1;
+    unsigned mask = 0;
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; k++)
+        if (id[k] >= 0 && id[k] < a.E) mask |= 1u << (id[k] / a.ep);
+    return mask;
+}
+
+__global__ void __launch_bounds__(kRingThreads) combine_partitioned_ring_kernel(PartArgs a, int NS) {
+    extern __shared__ __align__(128) unsigned char smem[];  // [NS][2H] rows | full[NS] | empty[NS]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t row_bytes = uint32_t(2 * a.H);
+    const uint32_t rows0 = smem_addr(smem), bars = rows0 + uint32_t(NS) * row_bytes;
+    if (tid == 0) {
+        for (int s = 0; s < NS; s++) {
+            mbar_init(bars + 8 * s, 1);
+            mbar_init(bars + 8 * (NS + s), kRingConsumerWarps);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    const int64_t G = gridDim.x;
+    const int64_t ntok = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / G + 1 : 0;
+    uint32_t cnt = 0;  // ring slots used so far (the same count in every warp)
+    bool ok = true;
+    if (warp == kRingConsumerWarps) {
+        // producer
+        unsigned lane_mask = 0;
+        for (int64_t i = 0; i < ntok && ok; i++) {
+            const int64_t t = blockIdx.x + i * G;
+            if ((i & 31) == 0) lane_mask = lane_token_partitions(a, i, ntok, lane);
+            unsigned mask = __shfl_sync(kFullMask, lane_mask, int(i & 31));
+            while (mask && ok) {
+                const int p = __ffs(mask) - 1;
+                mask &= mask - 1;
+                const int s = int(cnt % uint32_t(NS));
+                if (lane == 0) {
+                    if (cnt >= uint32_t(NS)) ok = mbar_wait(bars + 8 * (NS + s), ((cnt / NS) - 1) & 1);
+                    if (ok)
+                        bulk_load(rows0 + uint32_t(s) * row_bytes, a.partial + (int64_t(p) * a.S + t) * a.H, row_bytes,
+                                  bars + 8 * s);
+                }
+                ok = __shfl_sync(kFullMask, ok, 0);
+                if (ok) cnt++;
+            }
+        }
+        if (lane == 0) {
+            if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
+            // the loads still in flight land before the CTA releases its shared memory
+            for (uint32_t c = cnt > uint32_t(NS) ? cnt - NS : 0; c < cnt; c++)
+                mbar_wait(bars + 8 * (c % NS), (c / NS) & 1, kDrainLimitNs);
+        }
+        return;
+    }
+    // consumers: thread c owns the 8-column vectors c, c + 256, ...
+    const int nvec = a.H / 8, nct = kRingConsumerWarps * 32;
+    unsigned lane_mask = 0;
+    for (int64_t i = 0; i < ntok && ok; i++) {
+        const int64_t t = blockIdx.x + i * G;
+        if ((i & 31) == 0) lane_mask = lane_token_partitions(a, i, ntok, lane);
+        unsigned mask = __shfl_sync(kFullMask, lane_mask, int(i & 31));
+        float acc[kRingMaxVecs][8];
+#pragma unroll
+        for (int j = 0; j < kRingMaxVecs; j++)
+#pragma unroll
+            for (int e = 0; e < 8; e++) acc[j][e] = 0.0f;
+        while (mask) {
+            mask &= mask - 1;
+            const int s = int(cnt % uint32_t(NS));
+            ok = mbar_wait(bars + 8 * s, (cnt / NS) & 1);
+            if (!__all_sync(kFullMask, ok)) {
+                ok = false;
+                break;
+            }
+            const unsigned char* row = smem + size_t(s) * row_bytes;
+#pragma unroll
+            for (int j = 0; j < kRingMaxVecs; j++) {
+                const int v = tid + j * nct;
+                if (v < nvec) {
+                    float f[8];
+                    unpack8(*reinterpret_cast<const uint4*>(row + 16 * v), f);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) acc[j][e] += f[e];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bars + 8 * (NS + s)) : "memory");
+            cnt++;
+        }
+        if (!ok) break;
+        uint16_t* dst = a.out + t * a.H;
+#pragma unroll
+        for (int j = 0; j < kRingMaxVecs; j++) {
+            const int v = tid + j * nct;
+            if (v < nvec)
+                st_v4(dst + 8 * v, make_uint4(pack_bf16x2(acc[j][0], acc[j][1]), pack_bf16x2(acc[j][2], acc[j][3]),
+                                              pack_bf16x2(acc[j][4], acc[j][5]), pack_bf16x2(acc[j][6], acc[j][7])));
+        }
+    }
+    if (!ok && lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
+}
+
 template <typename Kernel>
 cudaError_t launch_units(const LaunchCtx& ctx, Kernel kern, const PartArgs& a, int64_t extra_threads) {
     int per_sm = 0;
@@ -381,6 +511,19 @@ cudaError_t launch_combine_partitioned(const LaunchCtx& ctx, const uint16_t* par
     a.units_per_row = (H + kSlice - 1) / kSlice;
     a.n_units = T * a.units_per_row;
     if (a.n_units == 0) return cudaSuccess;
+    // large batches whose rows fit a consumer thread's registers (H <= 8192): the ring
+    const size_t row_bytes = 2 * size_t(H);
+    const int NS = int(std::max<size_t>(kRingMinSlots, std::min<size_t>(kRingMaxSlots, kRingTargetBytes / row_bytes)));
+    if (T >= kRingMinTokens && H / 8 <= kRingMaxVecs * kRingConsumerWarps * 32) {
+        const size_t smem = size_t(NS) * row_bytes + 16 * size_t(NS);
+        cudaError_t err =
+            cudaFuncSetAttribute(combine_partitioned_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        int per_sm = 0;
+        if (err == cudaSuccess) err = blocks_per_sm(ctx, combine_partitioned_ring_kernel, kRingThreads, smem, &per_sm);
+        if (err != cudaSuccess) return err;
+        const int grid = int(std::min<int64_t>(T, int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1)));
+        return launch_pdl(ctx, combine_partitioned_ring_kernel, dim3(grid), dim3(kRingThreads), smem, a, NS);
+    }
     return launch_units(ctx, combine_partitioned_kernel, a, 0);
 }
 
