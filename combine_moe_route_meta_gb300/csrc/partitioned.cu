@@ -201,6 +201,158 @@ __global__ void __launch_bounds__(kThreads) dispatch_partitioned_kernel(PartArgs
     }
 }
 
+// NVFP4 with 128 x 4 swizzled scales when every 128-row tile lies in one partition (S % 128 ==
+// 0): the scale tiles are built in shared memory and written as whole 16-byte lines, so there is
+// neither a clear nor an interleave pass. Line L of a tile holds rows L, L+32, L+64 and L+96 (4
+// scale columns each), so the 128 slots of a group split into two halves that share no line: half
+// h takes the rows whose L lies in [16h, 16h + 16). Unit = (group of 128 tokens, half, 512-column
+// slice), 64 tokens: warp w quantises 8 of them (lane = 16 columns = one block; the row slices of
+// kTileBatch tokens in flight, the next batch loaded while the current one is quantised), stores
+// each token's codes (256 bytes) into the row of every partition it goes to and its block scales
+// into the 8 staged tiles of the slice. A token's scales are the same for every partition, and so
+// is their place in a tile (slot t sits at row t % 128 of its partition's tile), so one staged
+// copy serves all P partitions: the threads then write the half's 16-byte lines for every
+// partition, with the words of slots the partition does not receive (or past T) zeroed. The
+// receive ids and weights are written by the slice-0 units.
+constexpr int kTileTokens = 128;     // slots per tile
+constexpr int kTileThreads = 256;  // also one thread per e4m3 code for the ratio table
+constexpr int kTileUnitTokens = 64;  // one half of a group
+constexpr int kTileParts = kTileTokens / kTileUnitTokens;     // units per group
+constexpr int kTileLines = kTileUnitTokens / 4;               // lines of a tile per unit
+constexpr int kTileWarpTokens = kTileUnitTokens / (kTileThreads / 32);  // 8
+constexpr int kTileBatch = 4;
+constexpr int kTilesPerSlice = kSlice / 64;  // tile columns (4 scale columns of 16 elements each)
+// staged tile stride: 512 bytes + 16, so that the 8 tiles of a slice start in different banks
+constexpr int kTileStride = 528;
+
+// row in its group of token j (< kTileUnitTokens) of part h
+__device__ __forceinline__ int tile_half_row(int h, int j) {
+    return kTileLines * h + (j % kTileLines) + 32 * (j / kTileLines);
+}
+
+__global__ void __launch_bounds__(kTileThreads, 4) dispatch_partitioned_tiles_kernel(PartArgs a) {
+    __shared__ unsigned s_mask[kTileTokens];  // bit p: partition p receives the token of row i
+    __shared__ __align__(16) unsigned char s_tiles[kTilesPerSlice * kTileStride];
+    __shared__ float s_ratio[256];  // nvfp4_ratio of every e4m3 code
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    s_ratio[tid] = nvfp4_ratio(a.g, uint32_t(tid));  // read after the first barrier below
+    pdl_wait();
+    const int H = a.H, K = a.K, P = a.P;
+    const int C4 = H / 64;  // tile columns per 128-row block
+    const int nsl = a.units_per_row;
+    uint8_t* recv_q = static_cast<uint8_t*>(a.recv_x);
+    // padding slots t in [T, S): every partition's ids are the invalid id
+    {
+        const int64_t per_p = (a.S - a.T) * K;
+        for (int64_t j = int64_t(blockIdx.x) * blockDim.x + tid; j < per_p * P; j += int64_t(gridDim.x) * blockDim.x) {
+            const int64_t p = j / per_p, rem = j - p * per_p;
+            a.recv_ids[(p * a.S + a.T) * K + rem] = a.invalid_id;
+        }
+    }
+    const LaneSlice zero{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    for (int64_t u = blockIdx.x; u < a.n_units; u += gridDim.x) {
+        const int64_t gh = u / nsl;  // (group, part); the slices of one part are neighbours
+        const int c = int(u - gh * nsl);
+        const int64_t t0 = (gh / kTileParts) * kTileTokens;
+        const int h = int(gh % kTileParts);
+        const int ntg = a.T - t0 < kTileTokens ? int(a.T - t0) : kTileTokens;  // rows holding tokens
+        const int col = c * kSlice + lane * kLaneElems;
+        const bool active = col < H;
+        const int jw = warp * kTileWarpTokens;
+        // the first batch of row slices is in flight while the routing masks are built
+        LaneSlice sl[kTileBatch];
+#pragma unroll
+        for (int b = 0; b < kTileBatch; b++) {
+            const int i = tile_half_row(h, jw + b);
+            sl[b] = zero;
+            if (active && i < ntg) sl[b] = load_slice(a.x + (t0 + i) * H + col);
+        }
+        if (tid < kTileUnitTokens) {
+            const int i = tile_half_row(h, tid);
+            unsigned m = 0;
+            if (i < ntg) {
+                const int32_t* ip = a.ids + (t0 + i) * K;
+                bool bad = false;
+                for (int k = 0; k < K; k++) {
+                    const int e = __ldg(ip + k);
+                    if (e >= 0 && e < a.E)
+                        m |= 1u << (e / a.ep);
+                    else
+                        bad |= e != -1;
+                }
+                if (bad && c == 0) set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
+            }
+            s_mask[i] = m;
+        }
+        __syncthreads();
+        for (int jb = 0; jb < kTileWarpTokens; jb += kTileBatch) {
+            if (jb > 0) {
+#pragma unroll
+                for (int b = 0; b < kTileBatch; b++) {
+                    const int i = tile_half_row(h, jw + jb + b);
+                    if (active && i < ntg) sl[b] = load_slice(a.x + (t0 + i) * H + col);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < kTileBatch; b++) {
+                const int i = tile_half_row(h, jw + jb + b);
+                if (i >= ntg || !active) continue;
+                const LaneCodes q = quantise16_nvfp4_lut(sl[b], a.g, s_ratio);
+                unsigned m = s_mask[i];
+                while (m) {
+                    const int p = __ffs(m) - 1;
+                    m &= m - 1;
+                    st_v2(recv_q + (int64_t(p) * a.S + t0 + i) * (H / 2) + col / 2, make_uint2(q.q.x, q.q.y));
+                }
+                // scale column 4*(lane/4) + lane%4 of the slice, row i of the tile
+                s_tiles[(lane >> 2) * kTileStride + (i & 31) * 16 + (i >> 5) * 4 + (lane & 3)] = uint8_t(q.scale);
+            }
+        }
+        if (c == 0) {
+            // the receive ids (ids the partition does not own -> invalid_id) and weights (routed
+            // partitions only) of every partition's row of the unit's tokens
+            for (int jj = tid; jj < kTileUnitTokens * K; jj += kTileThreads) {
+                const int j = jj / K, k = jj - j * K;
+                const int i = tile_half_row(h, j);
+                if (i >= ntg) continue;
+                const int64_t t = t0 + i;
+                const int id = __ldg(a.ids + t * K + k);
+                const float w = __ldg(a.w + t * K + k);
+                const unsigned m = s_mask[i];
+                const bool valid = id >= 0 && id < a.E;
+                for (int p = 0; p < P; p++) {
+                    const bool rp = (m >> p) & 1u;
+                    const int64_t r = (int64_t(p) * a.S + t) * K + k;
+                    a.recv_ids[r] = (rp && valid && id / a.ep == p) ? id : a.invalid_id;
+                    if (rp) a.recv_w[r] = w;
+                }
+            }
+        }
+        __syncthreads();
+        // the part's lines of the slice's tiles: thread -> (tile q, line L), partitions p0,
+        // p0 + kPStep, ...
+        constexpr int kPStep = kTileThreads / (kTilesPerSlice * kTileLines);
+        const int nq = min(kTilesPerSlice, C4 - c * kTilesPerSlice);
+        const int q = (tid / kTileLines) % kTilesPerSlice, L = kTileLines * h + tid % kTileLines;
+        const int p0 = tid / (kTilesPerSlice * kTileLines);
+        if (q < nq) {
+            const uint4 v = *reinterpret_cast<const uint4*>(s_tiles + q * kTileStride + L * 16);
+            const unsigned m0 = s_mask[L], m1 = s_mask[L + 32], m2 = s_mask[L + 64], m3 = s_mask[L + 96];
+            const int64_t tile0 = (gh / kTileParts) * C4 + c * kTilesPerSlice + q;  // the tile of partition 0
+            const int64_t tiles_per_p = (a.S / kTileTokens) * C4;
+            for (int p = p0; p < P; p += kPStep) {
+                uint4 o;
+                o.x = (m0 >> p) & 1u ? v.x : 0u;
+                o.y = (m1 >> p) & 1u ? v.y : 0u;
+                o.z = (m2 >> p) & 1u ? v.z : 0u;
+                o.w = (m3 >> p) & 1u ? v.w : 0u;
+                st_v4(a.recv_sf + (tile0 + int64_t(p) * tiles_per_p) * 512 + L * 16, o);
+            }
+        }
+        __syncthreads();  // s_mask and s_tiles are rebuilt by the next unit
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs a) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
@@ -275,8 +427,9 @@ constexpr int kRingMaxSlots = 16;
 constexpr int kRingMinSlots = 2;
 constexpr int64_t kRingMinTokens = 1024;
 // Ring size: about 28 KB (two 14 KB rows at H = 7168). Measured on the nvfp4 tokens (P = 8): one
-// 200 KB ring per SM 141.3 us, 100 KB 137.2, 70 KB 131.1, 44 KB 129.0, 28 KB (seven CTAs per SM)
-// 127.0 us; four consumer warps instead of eight 128.0-129.0; a single slot 147.4 us.
+// 200 KB ring per SM 141.3 us, 100 KB 137.2, 70 KB 131.1, 44 KB 129.0, 28 KB 127.0 us (from 44 KB
+// down, four CTAs per SM, held there by 56 registers x 288 threads); four consumer warps instead
+// of eight 128.0-129.0; a single slot 147.4 us.
 constexpr size_t kRingTargetBytes = 28 * 1024;
 
 // Partitions of the CTA's tokens i0 + lane (stride G from blockIdx.x), one token per lane, as bit
@@ -451,7 +604,27 @@ cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const u
     a.units_per_row = (H + kSlice - 1) / kSlice;
     a.n_units = T * a.units_per_row;
     a.L = ScaleLayout{scale_layout, 0, 0};
-    // swizzled NVFP4 scales: when the buffer allows it, the scale rows go out row-major and the
+    // swizzled NVFP4 scales whose 128-row tiles each lie in one partition: one launch writes
+    // the codes and the whole tiles (dispatch_partitioned_tiles_kernel)
+    if (quant == MOE_QUANT_NVFP4_B16 && scale_layout == MOE_SCALES_SWIZZLED_128X4 && S % kTileTokens == 0 &&
+        (reinterpret_cast<uintptr_t>(recv_sf) & 15) == 0) {
+        a.n_units = (T + kTileTokens - 1) / kTileTokens * kTileParts * a.units_per_row;
+        const int64_t pad = (S - T) * P * K;
+        if (a.n_units == 0 && pad == 0) return cudaSuccess;
+        int per_sm = 0;
+        cudaError_t err = blocks_per_sm(ctx, dispatch_partitioned_tiles_kernel, kTileThreads, 0, &per_sm);
+        if (err != cudaSuccess) return err;
+        const int64_t cap = int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1);
+        // every CTA takes the same number of units
+        int64_t grid = std::min(cap, (pad + kTileThreads - 1) / kTileThreads);
+        if (a.n_units > 0) {
+            const int64_t per_cta = (a.n_units + cap - 1) / cap;
+            grid = (a.n_units + per_cta - 1) / per_cta;
+        }
+        return launch_pdl(ctx, dispatch_partitioned_tiles_kernel, dim3(unsigned(std::max<int64_t>(1, grid))),
+                          dim3(kTileThreads), 0, a);
+    }
+    // swizzled NVFP4 scales otherwise: when the buffer allows it, the scale rows go out row-major and the
     // touched tiles are interleaved in place afterwards (the interleave zeroing the rows the
     // dispatch does not write, or a clear of the touched tiles first where it cannot tell them);
     // else the touched tiles are cleared and every scale word is stored at its tile position

@@ -399,8 +399,10 @@ moe_status_t moe_dispatch_partitioned(moe_quant_t quant, const uint16_t *hidden_
  * t < T of some partition, and the one holding the padding rows, are written in full: slots a
  * partition does not receive are zero there, like the padding rows (moe_scale_layout_t); tiles
  * of padding slots only keep their bytes. NVFP4 only, H % 64 == 0, recv_scales 4-byte aligned.
- * Launches: a clear of the touched tiles, the dispatch, and (recv_scales 16-byte aligned) an
- * in-place interleave of the row-major scale rows the dispatch wrote there.
+ * Launches: with num_slots % 128 == 0 and recv_scales 16-byte aligned, one (every tile lies in
+ * one partition and is written whole from shared memory); otherwise a clear of the touched
+ * tiles, the dispatch, and (recv_scales 16-byte aligned) an in-place interleave of the
+ * row-major scale rows the dispatch wrote there.
  * MOE_SCALES_ROW_MAJOR is moe_dispatch_partitioned.
  * Everything else as moe_dispatch_partitioned.
  */

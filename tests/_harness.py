@@ -296,3 +296,34 @@ def run_full_large(w: Workload, *, expert_seed: int = 4321):
     assert int(st3.item()) == 0
     check_combine(bytes_of(out).view(np.uint16).reshape(w.T, w.H), want)
     return om
+
+
+def run_partitioned_dispatch(w: Workload, P: int, S: int, layout: str, invalid_id: int = -1):
+    """moe_dispatch_partitioned_ex of an NVFP4 workload against oracle.dispatch_partitioned, in
+    full: every receive code row (untouched rows keep the fill), the scales (row-major, or the
+    swizzled layout's expected bytes), ids and weights, and the status word."""
+    m = moe()
+    x, ids, wt = to_dev(w)
+    H, E, K = w.H, w.E, w.K
+    g = w.global_scale if w.global_scale is not None else 0.0
+    rx = filled((P, S, H // 2), torch.uint8)
+    rsf = filled((m.swizzled_scale_bytes(P * S, H),) if layout == "swizzled" else (P, S, H // 16), torch.uint8)
+    rids = filled((P, S, K), torch.int32)
+    rw = filled((P, S, K), torch.float32)
+    st = m.new_status()
+    m.moe_dispatch_partitioned_ex("nvfp4b16", layout, x, ids, wt, E, P, rx, rsf, rids, rw, st,
+                                  invalid_expert_id=invalid_id, input_global_scale=g)
+    ox, osf, oids, ow = oracle.dispatch_partitioned("nvfp4b16", w.x, w.topk_ids, w.topk_weights, E, P,
+                                                    invalid_id=invalid_id, global_scale=g, num_slots=S, fill=SENTINEL)
+    torch.cuda.synchronize()
+    assert np.array_equal(bytes_of(rx).reshape(-1), np.ascontiguousarray(ox).view(np.uint8).reshape(-1)), "codes"
+    if layout == "swizzled":
+        want = swizzled_scales_expected(osf.reshape(P * S, H // 16), partitioned_routed(w.topk_ids, E, P, S),
+                                        partitioned_touched_rows(P, S, w.T))
+    else:
+        want = osf
+    assert np.array_equal(rsf.cpu().numpy().reshape(-1), np.asarray(want).reshape(-1)), "scales"
+    assert np.array_equal(rids.cpu().numpy(), oids), "ids"
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32)), "weights"
+    assert int(st.item()) == 0
+    check_guards()

@@ -11,7 +11,7 @@ import pytest
 
 from workloads import make_case
 
-from _harness import run_full
+from _harness import run_full, run_partitioned_dispatch
 
 pytestmark = pytest.mark.gpu
 
@@ -62,3 +62,18 @@ def test_nvfp4_degenerate_global_scales(g, mode, M):
     w = make_case(24, 512, 8, 2, seed=93, mode=mode, quant="nvfp4b16", M=M)
     w = _with_rows(w, _extreme_rows(w.H, np.random.default_rng(94), huge=False))
     run_full(dataclasses.replace(w, global_scale=g))
+
+
+@pytest.mark.parametrize("g", [1.0, 0.0, 1e-30, 1e30])
+@pytest.mark.parametrize("layout,T,S", [("swizzled", 24, 128), ("row", 24, 24), ("swizzled", 1100, 1152),
+                                        ("row", 1100, 1100)])
+def test_partitioned_nvfp4_extreme_values(g, layout, T, S):
+    """The same degenerate rows and global scales through the FlashInfer partition layout: the
+    kernel that builds whole swizzled tiles (num_slots % 128 == 0) has a quantiser of its own."""
+    w = make_case(T, 512, 16, 4, seed=93, quant="nvfp4b16")
+    rows = _extreme_rows(w.H, np.random.default_rng(94), huge=True)
+    x = w.x.copy()
+    for i, r in enumerate(rows):
+        x[(i * 137) % T] = r
+    w = dataclasses.replace(w, x=x, global_scale=g)
+    run_partitioned_dispatch(w, 4, S, layout)

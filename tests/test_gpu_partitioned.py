@@ -138,6 +138,11 @@ def test_partitioned_nvfp4_workload_in_full(layout):
     (128, 128, 7168, 256, 8, 8),      # the FlashInfer NVFP4 payload shape, 1024 rows
     (1100, 1130, 2048, 64, 8, 8),     # >= 1024 tokens: the bulk kernel, padding slots
     (1030, 1030, 256, 96, 6, 32),     # bulk kernel, 32 partitions, 32960 rows -> padded to 33024
+    # num_slots % 128 == 0: every tile lies in one partition and is built whole in shared memory
+    (1000, 1024, 1088, 64, 8, 8),     # ragged last token group (104 slots) and last column slice (1 tile)
+    (300, 512, 256, 96, 6, 32),       # 32 partitions; the last slot group of each partition untouched
+    (0, 128, 64, 4, 2, 1),            # no tokens: padding ids only, no tile touched
+    (4096, 4096, 4096, 128, 8, 4),    # many units per CTA
 ])
 def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
     """moe_dispatch_partitioned_ex with swizzled scales equals the row-major receive scales
@@ -154,6 +159,36 @@ def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
     rw = filled((P, S, K), torch.float32)
     st = m.new_status()
     m.moe_dispatch_partitioned_ex("nvfp4b16", "swizzled", x, ids, wt, E, P, rx, rsf, rids, rw, st,
+                                  input_global_scale=w.global_scale or 0.0)
+    ox, osf, oids, ow = oracle.dispatch_partitioned("nvfp4b16", w.x, w.topk_ids, w.topk_weights, E, P,
+                                                    global_scale=w.global_scale or 0.0, num_slots=S, fill=SENTINEL)
+    torch.cuda.synchronize()
+    assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
+    want = swizzled_scales_expected(osf.reshape(P * S, H // 16), partitioned_routed(w.topk_ids, E, P, S),
+                                    partitioned_touched_rows(P, S, T))
+    assert np.array_equal(rsf.cpu().numpy(), want)
+    assert np.array_equal(rids.cpu().numpy(), oids)
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
+    assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("T,S,offset", [(200, 256, 4), (1100, 1152, 12)])
+def test_partitioned_swizzled_scales_unaligned_buffer(T, S, offset):
+    """A swizzled receive-scale buffer that is 4- but not 16-byte aligned (num_slots a multiple
+    of 128): the tiles are cleared and the scale words stored one by one, with the same bytes as
+    nvfp4_block_scale_interleave of the row-major receive scales."""
+    m = moe()
+    H, E, K, P = 1024, 64, 8, 8
+    w = make_case(T, H, E, K, seed=T + offset, quant="nvfp4b16", invalid_rate=0.05)
+    x, ids, wt = to_dev(w)
+    rx = filled((P, S, H // 2), torch.uint8)
+    nsf = m.swizzled_scale_bytes(P * S, H)
+    base = filled((nsf + 16,), torch.uint8)
+    rsf = base[offset:offset + nsf]
+    rids = filled((P, S, K), torch.int32)
+    rw = filled((P, S, K), torch.float32)
+    st = m.new_status()
+    m.moe_dispatch_partitioned_ex("nvfp4b16", "swizzled", x, ids, wt, E, P, rx, rsf, rids, rw, st,
                                   input_global_scale=w.global_scale)
     ox, osf, oids, ow = oracle.dispatch_partitioned("nvfp4b16", w.x, w.topk_ids, w.topk_weights, E, P,
                                                     global_scale=w.global_scale, num_slots=S, fill=SENTINEL)
@@ -161,7 +196,9 @@ def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
     assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
     want = swizzled_scales_expected(osf.reshape(P * S, H // 16), partitioned_routed(w.topk_ids, E, P, S),
                                     partitioned_touched_rows(P, S, T))
-    assert np.array_equal(rsf.cpu().numpy(), want)
+    got = base.cpu().numpy()
+    assert np.array_equal(got[offset:offset + nsf], want)
+    assert np.all(got[:offset] == SENTINEL) and np.all(got[offset + nsf:] == SENTINEL)
     assert np.array_equal(rids.cpu().numpy(), oids)
     assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
     assert int(st.item()) == 0
