@@ -201,6 +201,47 @@ __global__ void __launch_bounds__(kThreads) dispatch_partitioned_kernel(PartArgs
     }
 }
 
+// The NVFP4 quantiser's per-block ratio g / value(sf) for the e4m3 code sf: the same correctly
+// rounded quotient quantise16 divides out per block (0 for the two zero codes, whose blocks get
+// zero codes). A kernel that tabulates it for all 256 codes once replaces a division per block
+// by a shared-memory load (quantise16_nvfp4_lut).
+__device__ __forceinline__ float nvfp4_ratio(float g, uint32_t code) {
+    const float sff = e4m3_value(code);
+    return sff != 0.0f ? __fdiv_rn(g, sff) : 0.0f;
+}
+
+// quantise16<MOE_QUANT_NVFP4_B16> with the ratio looked up in s_ratio[256] (nvfp4_ratio of
+// every code) and the block amax taken on the packed bf16 pairs (abs and max of bf16 values
+// are exact, and max returns the non-NaN operand as fmaxf does): the same codes and scale.
+__device__ __forceinline__ LaneCodes quantise16_nvfp4_lut(const LaneSlice& s, float g, const float* s_ratio) {
+    uint32_t m;
+    asm("{\n\t.reg .b32 a, b, c, d;\n\t"
+        "abs.bf16x2 a, %1;\n\tabs.bf16x2 b, %2;\n\tabs.bf16x2 c, %3;\n\tabs.bf16x2 d, %4;\n\t"
+        "max.bf16x2 a, a, b;\n\tmax.bf16x2 c, c, d;\n\tmax.bf16x2 a, a, c;\n\t"
+        "abs.bf16x2 b, %5;\n\tabs.bf16x2 c, %6;\n\tabs.bf16x2 d, %7;\n\t"
+        "max.bf16x2 a, a, b;\n\tmax.bf16x2 c, c, d;\n\tmax.bf16x2 a, a, c;\n\t"
+        "abs.bf16x2 b, %8;\n\tmax.bf16x2 %0, a, b;\n\t}"
+        : "=r"(m)
+        : "r"(s.v0.x), "r"(s.v0.y), "r"(s.v0.z), "r"(s.v0.w), "r"(s.v1.x), "r"(s.v1.y), "r"(s.v1.z), "r"(s.v1.w));
+    const float amax = fmaxf(fmaxf(bf16_lo(m), bf16_hi(m)), 0.0f);  // 0 when all 16 are NaN, as in quantise16
+    const float tsf = __fmul_rn(__fdiv_rn(amax, 6.0f), g);
+    LaneCodes out;
+    out.scale = e4m3x2(tsf, 0.0f) & 0xffu;
+    out.q = make_uint4(0, 0, 0, 0);
+    if (out.scale & 0x7fu) {  // not one of the two zero codes
+        const float r = s_ratio[out.scale];
+        float f[16];
+        unpack8(s.v0, f);
+        unpack8(s.v1, f + 8);
+        uint32_t b[8];
+#pragma unroll
+        for (int p = 0; p < 8; p++) b[p] = e2m1x2(__fmul_rn(f[2 * p], r), __fmul_rn(f[2 * p + 1], r));
+        out.q.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+        out.q.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+    }
+    return out;
+}
+
 // NVFP4 with 128 x 4 swizzled scales when every 128-row tile lies in one partition (S % 128 ==
 // 0): the scale tiles are built in shared memory and written as whole 16-byte lines, so there is
 // neither a clear nor an interleave pass. Line L of a tile holds rows L, L+32, L+64 and L+96 (4
