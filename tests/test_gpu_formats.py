@@ -7,9 +7,9 @@ import pytest
 import torch
 
 import oracle
-from workloads import make_case, random_bf16
+from workloads import make_case, make_workload, random_bf16
 
-from _harness import (SENTINEL, bytes_of, check_combine, filled, masked_rows, masked_touched_rows, moe, to_dev,
+from _harness import (_all_bytes_are, _sentinel_buffer, SENTINEL, bytes_of, check_combine, filled, masked_rows, masked_touched_rows, moe, to_dev,
                       swizzled_scales_expected)
 
 pytestmark = pytest.mark.gpu
@@ -313,3 +313,57 @@ def _swizzled_case(mode, T, H, E, K, M, offset):
     assert np.array_equal(bytes_of(q).reshape(-1), oq.reshape(-1))
     assert np.array_equal(sf.cpu().numpy(), want_sf)
     assert int(st.item()) == 0    # the dispatch drops pairs past capacity silently (route_meta reports them)
+
+
+def test_nvfp4_masked_swizzled_workload_in_full():
+    """The nvfp4 workload (T=8192, H=7168, E=256, K=8, M=8192) with swizzled scales, in the
+    benchmark's launch configuration: every written code row against the oracle; every touched
+    128-row block of the [E*M, H/16] scale matrix equal to the oracle's interleave of its
+    expected rows (the expert's scale rows, zeros below the block's end); every other byte of
+    both buffers still the fill. The host builds the touched blocks only (the buffers are
+    7.5 GB and 0.9 GB)."""
+    m = moe()
+    w = make_workload("nvfp4")
+    x, ids, _ = to_dev(w)
+    E, M, H, K = w.E, w.M, w.H, w.K
+    C = H // 16
+    om = oracle.route_meta(w.topk_ids, E, M=M)
+    seg = torch.from_numpy(om.seg_indptr).cuda()
+    s2d = torch.from_numpy(om.src2dst).cuda()
+    R = E * M
+    q = _sentinel_buffer((R, H // 2), torch.uint8)
+    nsf = m.swizzled_scale_bytes(R, H)
+    assert nsf == R * C
+    sf = _sentinel_buffer((nsf,), torch.uint8)
+    st = m.new_status()
+    m.moe_dispatch_ex("masked", "nvfp4b16", "swizzled", x, ids, E, s2d, seg, q, sf, st, max_tokens_per_expert=M,
+                      input_global_scale=w.global_scale)
+    n = om.num_valid
+    valid = om.src2dst >= 0
+    pair_of_slot = np.empty(n, np.int64)
+    pair_of_slot[om.src2dst[valid]] = np.nonzero(valid)[0]
+    dst = masked_rows(w, om)[pair_of_slot]        # masked row of contiguous slot j
+    assert (dst >= 0).all()
+    oq, osc = oracle.dispatch("normal", "nvfp4b16", w.x, w.topk_ids, om, E, global_scale=w.global_scale, rows=n)
+    osc = np.ascontiguousarray(osc[:n]).view(np.uint8).reshape(n, C)
+    dst_d = torch.from_numpy(dst).cuda()
+    got = q.index_select(0, dst_d)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(got.cpu().numpy(), np.ascontiguousarray(oq[:n]).view(np.uint8).reshape(n, -1)), "codes"
+    q.index_fill_(0, dst_d, SENTINEL)
+    assert _all_bytes_are(q, SENTINEL), "rows no pair maps to were written"
+    del q, got
+
+    blk = np.unique(np.nonzero(masked_touched_rows(om.seg_indptr, E, M))[0] // 128)
+    slot_of_row = np.full(R, -1, np.int64)
+    slot_of_row[dst] = np.arange(n)
+    sl = slot_of_row[(blk[:, None] * 128 + np.arange(128)).reshape(-1)]
+    rows = np.zeros((blk.size * 128, C), np.uint8)
+    rows[sl >= 0] = osc[sl[sl >= 0]]
+    want = oracle.nvfp4_sf_interleave(rows).reshape(blk.size, 128 * C)
+    sf2 = sf.view(R // 128, 128 * C)
+    blk_d = torch.from_numpy(blk).cuda()
+    assert np.array_equal(sf2.index_select(0, blk_d).cpu().numpy(), want), "touched scale blocks"
+    sf2.index_fill_(0, blk_d, SENTINEL)
+    assert _all_bytes_are(sf2, SENTINEL), "untouched scale blocks were written"

@@ -90,16 +90,18 @@ def test_partitioned_dispatch_and_combine_match_oracle(T, S, H, E, K, P, quant, 
     check_combine(bytes_of(out).view(np.uint16).reshape(T, H), want)
 
 
-@pytest.mark.parametrize("layout", ["row", "swizzled"])
+@pytest.mark.parametrize("layout", ["row", "swizzled", "swizzled_pad"])
 def test_partitioned_nvfp4_workload_in_full(layout):
     """The nvfp4 workload (T=8192, H=7168, E=256, K=8, P=8, one receive slot per token) through
     the FlashInfer layout, in the benchmark's launch configuration: every receive row, scale,
     sanitised id and weight (row-major or swizzled scales), the untouched payload of slots a
-    partition does not receive, and every element of the partitioned combine."""
+    partition does not receive, and every element of the partitioned combine. swizzled_pad: 64
+    padding slots per partition, so that tiles straddle partitions (the interleave pass)."""
     m = moe()
     w = make_workload("nvfp4")
     x, ids, wt = to_dev(w)
-    P, S, K, H, E = w.P, w.T, w.K, w.H, w.E
+    P, S, K, H, E = w.P, w.T + (64 if layout == "swizzled_pad" else 0), w.K, w.H, w.E
+    layout = "swizzled" if layout.startswith("swizzled") else layout
     rx = filled((P, S, H // 2), torch.uint8)
     rsf = filled((m.swizzled_scale_bytes(P * S, H),) if layout == "swizzled" else (P, S, H // 16), torch.uint8)
     rids = filled((P, S, K), torch.int32)
