@@ -265,6 +265,11 @@ constexpr int kTileBatch = 4;
 constexpr int kTilesPerSlice = kSlice / 64;  // tile columns (4 scale columns of 16 elements each)
 // staged tile stride: 512 bytes + 16, so that the 8 tiles of a slice start in different banks
 constexpr int kTileStride = 528;
+static_assert(kTileThreads == 256, "one thread per e4m3 code fills the ratio table");
+static_assert(kTileUnitTokens % 4 == 0 && 32 % kTileLines == 0 && kTileUnitTokens <= kTileThreads,
+              "a unit is whole lines of a tile, its masks built by one thread per token");
+static_assert(kTileWarpTokens % kTileBatch == 0, "whole batches per warp");
+static_assert(kTileThreads % (kTilesPerSlice * kTileLines) == 0, "whole partition phases in the tile output");
 
 // row in its group of token j (< kTileUnitTokens) of part h
 __device__ __forceinline__ int tile_half_row(int h, int j) {
