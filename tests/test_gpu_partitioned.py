@@ -145,6 +145,7 @@ def test_partitioned_nvfp4_workload_in_full(layout):
     (300, 512, 256, 96, 6, 32),       # 32 partitions; the last slot group of each partition untouched
     (0, 128, 64, 4, 2, 1),            # no tokens: padding ids only, no tile touched
     (4096, 4096, 4096, 128, 8, 4),    # many units per CTA
+    (700, 768, 512, 64, 16, 16),      # top-16, 16 partitions
 ])
 def test_partitioned_swizzled_scales_match_oracle_interleave(T, S, H, E, K, P):
     """moe_dispatch_partitioned_ex with swizzled scales equals the row-major receive scales
