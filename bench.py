@@ -861,7 +861,8 @@ def next_rows_f1(args, dev, st, timed_us, emit, dev_in):
                                                      input_global_scale=g)
         us = timed_us(fn)
         emit("f1", f"moe_dispatch_partitioned_ex({quant}, {layout} scales)", "nvfp4", T, us, nbytes,
-             ["dispatch_partitioned_tiles_kernel"] if layout == "swizzled" else ["dispatch_bulk_quant_kernel"], 1)
+             ["dispatch_partitioned_tiles_kernel"] if layout == "swizzled" else
+             (["dispatch_partitioned_ring_kernel"] if quant == "nvfp4b16" else ["dispatch_bulk_copy_kernel"]), 1)
         del rx, rsf, rids, rw
     partial = torch.randn((P, S, H), dtype=torch.bfloat16, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)

@@ -399,6 +399,172 @@ __global__ void __launch_bounds__(kTileThreads, 4) dispatch_partitioned_tiles_ke
     }
 }
 
+// NVFP4 with row-major scales, >= 1024 tokens: the dispatch as a warp-specialised ring. Warp 0
+// (producer) bulk-copies token rows into kDRingIn row slots, kDRingIn tokens ahead. Warps
+// 2 .. 2+kDRingConsumerWarps-1 (consumers) quantise a token's 16-element blocks from its row slot
+// into one of kDRingOut code-row slots (codes, then the row's scales). Warp 1 (stores) finds the
+// partitions each token goes to, writes the receive ids and weights of its P rows, and once the
+// code row is complete stores it, with its scale row, to every routed partition by bulk copies.
+// Full / empty mbarriers hand each slot from one role to the next (row slot: producer ->
+// consumers -> producer; code-row slot: consumers -> stores -> consumers), so no role waits on a
+// block-wide barrier. Every wait is bounded; a role that gives up reports MOE_ERR_TIMEOUT and
+// the others give up in turn.
+constexpr int kDRingConsumerWarps = 7;  // 224 threads: two passes over a 7168-element row
+constexpr int kDRingThreads = (2 + kDRingConsumerWarps) * 32;
+constexpr int kDRingIn = 2;
+constexpr int kDRingOut = 3;
+
+size_t dring_smem(int H) {
+    return size_t(kDRingIn) * 2 * H + size_t(kDRingOut) * (H / 2 + H / 16) + 8 * 2 * (kDRingIn + kDRingOut);
+}
+
+__global__ void __launch_bounds__(kDRingThreads) dispatch_partitioned_ring_kernel(PartArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = a.H, K = a.K, P = a.P;
+    const uint32_t in_bytes = uint32_t(2 * H), qb = uint32_t(H / 2), sb = uint32_t(H / 16), ob = qb + sb;
+    const uint32_t in0 = smem_addr(smem), out0 = in0 + kDRingIn * in_bytes;
+    const uint32_t bars = out0 + kDRingOut * ob;
+    auto in_full = [&](int s) { return bars + 8 * s; };
+    auto in_empty = [&](int s) { return bars + 8 * (kDRingIn + s); };
+    auto out_full = [&](int o) { return bars + 8 * (2 * kDRingIn + o); };
+    auto out_empty = [&](int o) { return bars + 8 * (2 * kDRingIn + kDRingOut + o); };
+    if (tid == 0) {
+        for (int s = 0; s < kDRingIn; s++) {
+            mbar_init(in_full(s), 1);
+            mbar_init(in_empty(s), kDRingConsumerWarps);
+        }
+        for (int o = 0; o < kDRingOut; o++) {
+            mbar_init(out_full(o), kDRingConsumerWarps);
+            mbar_init(out_empty(o), 1);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    pdl_wait();
+    // padding slots t in [T, S): every partition's ids are the invalid id
+    {
+        const int64_t per_p = (a.S - a.T) * K;
+        for (int64_t j = int64_t(blockIdx.x) * blockDim.x + tid; j < per_p * P; j += int64_t(gridDim.x) * blockDim.x) {
+            const int64_t p = j / per_p, rem = j - p * per_p;
+            a.recv_ids[(p * a.S + a.T) * K + rem] = a.invalid_id;
+        }
+    }
+    const int64_t G = gridDim.x;
+    const int64_t ntok = a.T > blockIdx.x ? (a.T - 1 - blockIdx.x) / G + 1 : 0;
+    if (warp == 0) {
+        // producer
+        if (lane == 0) {
+            bool ok = true;
+            int64_t issued = 0;
+            for (int64_t i = 0; i < ntok; i++) {
+                const int s = int(i % kDRingIn);
+                if (i >= kDRingIn) ok = mbar_wait(in_empty(s), uint32_t((i / kDRingIn - 1) & 1));
+                if (!ok) break;
+                bulk_load(in0 + s * in_bytes, a.x + (blockIdx.x + i * G) * H, in_bytes, in_full(s));
+                issued = i + 1;
+            }
+            if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
+            // the copies still in flight land before the CTA's shared memory is released
+            for (int64_t j = issued > kDRingIn ? issued - kDRingIn : 0; j < issued; j++)
+                mbar_wait(in_full(int(j % kDRingIn)), uint32_t((j / kDRingIn) & 1), kDrainLimitNs);
+        }
+        return;
+    }
+    if (warp == 1) {
+        // stores: routing, receive ids and weights, bulk stores of the code and scale rows
+        uint8_t* recv_q = static_cast<uint8_t*>(a.recv_x);
+        int nid = -1;
+        float nw = 0.0f;
+        if (ntok > 0 && lane < K) {
+            nid = __ldg(a.ids + int64_t(blockIdx.x) * K + lane);
+            nw = __ldg(a.w + int64_t(blockIdx.x) * K + lane);
+        }
+        bool ok = true;
+        const int rounds = (P * K + 31) / 32;
+        for (int64_t i = 0; i < ntok; i++) {
+            const int64_t t = blockIdx.x + i * G;
+            const int o = int(i % kDRingOut);
+            const int my_id = nid;
+            const float my_w = nw;
+            if (i + 1 < ntok && lane < K) {  // the next token's ids and weights, one token ahead
+                nid = __ldg(a.ids + (t + G) * K + lane);
+                nw = __ldg(a.w + (t + G) * K + lane);
+            }
+            const bool valid = my_id >= 0 && my_id < a.E;
+            if (!valid && my_id != -1 && lane < K) set_status(a.status, MOE_ERR_BAD_EXPERT_ID);
+            bool routed = false;
+            for (int k = 0; k < K; k++) {
+                const int e = __shfl_sync(kFullMask, my_id, k);
+                routed |= e >= 0 && e < a.E && e / a.ep == lane;
+            }
+            const unsigned mask = __ballot_sync(kFullMask, routed && lane < P);
+            for (int r = 0; r < rounds; r++) {
+                const int j = r * 32 + lane;
+                const int p = j / K, k = j - p * K;
+                const int id = __shfl_sync(kFullMask, my_id, k & 31);
+                const float wk = __shfl_sync(kFullMask, my_w, k & 31);
+                if (j < P * K) {
+                    const bool rp = (mask >> p) & 1u;
+                    const int64_t rr = (int64_t(p) * a.S + t) * K + k;
+                    a.recv_ids[rr] = (rp && id >= 0 && id < a.E && id / a.ep == p) ? id : a.invalid_id;
+                    if (rp) a.recv_w[rr] = wk;
+                }
+            }
+            int got = 1;
+            if (lane == 0) got = mbar_wait(out_full(o), uint32_t((i / kDRingOut) & 1));
+            ok = __shfl_sync(kFullMask, got, 0) != 0;
+            if (!ok) break;
+            if (lane == 0) {
+                for (unsigned m = mask; m; m &= m - 1) {
+                    const int64_t row = int64_t(__ffs(m) - 1) * a.S + t;
+                    bulk_store(recv_q + row * qb, out0 + o * ob, qb);
+                    bulk_store(a.recv_sf + row * sb, out0 + o * ob + qb, sb);
+                }
+                bulk_commit();
+                // the stores of token i - (kDRingOut - 1) have read their slot: hand it back
+                bulk_wait_read<kDRingOut - 1>();
+                if (i >= kDRingOut - 1)
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(out_empty(int((i - kDRingOut + 1) % kDRingOut)))
+                                 : "memory");
+            }
+        }
+        if (lane == 0) {
+            bulk_wait_all();
+            if (!ok) set_status(a.status, MOE_ERR_TIMEOUT);
+        }
+        return;
+    }
+    // consumers: thread ct quantises the 16-element blocks ct, ct + nct, ... of each row
+    const int ct = tid - 64, nct = kDRingConsumerWarps * 32, nslices = H / 16;
+    bool ok = true;
+    for (int64_t i = 0; i < ntok; i++) {
+        const int s = int(i % kDRingIn), o = int(i % kDRingOut);
+        ok = mbar_wait(in_full(s), uint32_t((i / kDRingIn) & 1));
+        if (ok && i >= kDRingOut) ok = mbar_wait(out_empty(o), uint32_t((i / kDRingOut - 1) & 1));
+        if (!__all_sync(kFullMask, ok)) {
+            ok = false;
+            break;
+        }
+        const unsigned char* src = smem + size_t(s) * in_bytes;
+        unsigned char* qo = smem + size_t(kDRingIn) * in_bytes + size_t(o) * ob;
+        for (int slice = ct; slice < nslices; slice += nct) {
+            const LaneSlice sl{*reinterpret_cast<const uint4*>(src + slice * 32),
+                               *reinterpret_cast<const uint4*>(src + slice * 32 + 16)};
+            const LaneCodes c = quantise16<MOE_QUANT_NVFP4_B16>(sl, a.g);
+            *reinterpret_cast<uint2*>(qo + slice * 8) = make_uint2(c.q.x, c.q.y);
+            qo[qb + slice] = uint8_t(c.scale);
+        }
+        fence_proxy_async();  // this thread's code and scale bytes become visible to the bulk stores
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(in_empty(s)) : "memory");
+            asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(out_full(o)) : "memory");
+        }
+    }
+    if (!ok && lane == 0) set_status(a.status, MOE_ERR_TIMEOUT);
+}
+
 __global__ void __launch_bounds__(kThreads) combine_partitioned_kernel(PartArgs a) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
@@ -698,6 +864,21 @@ cudaError_t launch_dispatch_partitioned(const LaunchCtx& ctx, int quant, const u
             scale_layout = MOE_SCALES_ROW_MAJOR;
             a.L.kind = MOE_SCALES_ROW_MAJOR;
         }
+    }
+    // NVFP4 with row-major scale rows (the caller's layout, not the swizzled layout's row-major
+    // stage) that bulk copies can store: the warp-specialised ring
+    constexpr bool kDRing = true;
+    if (kDRing && quant == MOE_QUANT_NVFP4_B16 && scale_layout == MOE_SCALES_ROW_MAJOR && !by_tiles && T >= 1024 &&
+        H % 256 == 0 &&
+        (reinterpret_cast<uintptr_t>(recv_sf) & 15) == 0 && dring_smem(H) <= 200 * 1024) {
+        const size_t smem = dring_smem(H);
+        cudaError_t err = cudaFuncSetAttribute(dispatch_partitioned_ring_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        int per_sm = 0;
+        if (err == cudaSuccess) err = blocks_per_sm(ctx, dispatch_partitioned_ring_kernel, kDRingThreads, smem, &per_sm);
+        if (err != cudaSuccess) return err;
+        const int grid = int(std::min<int64_t>(T, int64_t(ctx.num_sms) * (per_sm > 0 ? per_sm : 1)));
+        return launch_pdl(ctx, dispatch_partitioned_ring_kernel, dim3(grid), dim3(kDRingThreads), smem, a);
     }
     bool bulk = false;
     cudaError_t err = launch_dispatch_partitioned_bulk(ctx, quant, x, T, S, H, ids, w, K, E, P, invalid_id, g,
