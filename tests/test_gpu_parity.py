@@ -175,16 +175,17 @@ def test_zero_rows_quantise_to_zero_codes():
         run_full(w)
 
 
-def test_capacity_overflow_drops_late_pairs_and_reports():
-    m = moe()
-    w = make_case(400, 256, 4, 2, seed=9, mode="masked", quant="fp8g128", M=100)
+@pytest.mark.parametrize("T,M", [(400, 100), (1600, 300)])  # register / ring (>= 1024 tokens) combine
+def test_capacity_overflow_drops_late_pairs_and_reports(T, M):
+    w = make_case(T, 256, 4, 2, seed=9, mode="masked", quant="fp8g128", M=M)
     om = run_full(w)
     assert om.status == oracle.CAPACITY
-    assert (om.masked_m == 100).any()
+    assert (om.masked_m == M).any()
 
 
-def test_out_of_range_ids_are_skipped_and_reported():
-    w = make_case(300, 256, 16, 4, seed=10, bad_rate=0.02, invalid_rate=0.02)
+@pytest.mark.parametrize("T,mode,M", [(300, "normal", 0), (1500, "normal", 0), (1500, "masked", 1500)])
+def test_out_of_range_ids_are_skipped_and_reported(T, mode, M):
+    w = make_case(T, 256, 16, 4, seed=10, mode=mode, M=M, bad_rate=0.02, invalid_rate=0.02)
     om = run_full(w)
     assert om.status == oracle.BAD_ID
 
