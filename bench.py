@@ -922,7 +922,7 @@ def next_rows_f3f4(dev, st, timed_us, emit, dev_in):
     sc = torch.empty(((G + 3) // 4, R4, 4), dtype=torch.uint8, device=dev)
     fn = lambda: moe.moe_dispatch_ex("normal", "fp8g128_ue8m0", "col", x, i32, E, s2d, seg, q, sc, st, out_rows=cap)
     emit("f3", "moe_dispatch_ex(fp8g128_ue8m0, column-major scales, aligned segments)", "prefill", T,
-         timed_us(fn), 2 * T * H + 4 * T * K + n_valid * (H + G), ["dispatch_kernel"], 1)
+         timed_us(fn), 2 * T * H + 4 * T * K + n_valid * (H + G), ["dispatch_bulk_quant_kernel"], 1)
     codes = torch.randint(0, 256, (T, H), dtype=torch.uint8, device=dev)
     om = moe.route_meta(ids, E, dev_status=st)
     fn = lambda: moe.moe_dispatch_ex("normal", "fp8_passthrough", "row", codes, ids, E, om.src2dst, om.seg_indptr,
