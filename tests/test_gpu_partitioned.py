@@ -13,6 +13,7 @@ import oracle
 from workloads import make_case, make_workload, random_bf16
 
 from _harness import (SENTINEL, bytes_of, check_combine, filled, moe, partitioned_routed, partitioned_touched_rows,
+                      run_partitioned_dispatch,
                       swizzled_scales_expected, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -205,3 +206,13 @@ def test_partitioned_swizzled_scales_unaligned_buffer(T, S, offset):
     assert np.array_equal(rids.cpu().numpy(), oids)
     assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("P,K,layout", [(1, 8, "row"), (4, 8, "row"), (16, 8, "row"), (32, 16, "row"),
+                                        (4, 8, "swizzled"), (32, 16, "swizzled")])
+def test_partitioned_nvfp4_ring_and_tiles_across_partition_counts(P, K, layout):
+    """2048 tokens of the nvfp4 shape (H = 7168, E = 256) through the ring dispatch (row-major
+    scales) and the whole-tile dispatch (swizzled, num_slots = T), from one partition to 32 and
+    up to top-16: every receive row, scale, id and weight against the oracle."""
+    w = make_case(2048, 7168, 256, K, seed=P * 31 + K, quant="nvfp4b16", invalid_rate=0.03)
+    run_partitioned_dispatch(w, P, w.T, layout)
