@@ -216,3 +216,32 @@ def test_partitioned_nvfp4_ring_and_tiles_across_partition_counts(P, K, layout):
     up to top-16: every receive row, scale, id and weight against the oracle."""
     w = make_case(2048, 7168, 256, K, seed=P * 31 + K, quant="nvfp4b16", invalid_rate=0.03)
     run_partitioned_dispatch(w, P, w.T, layout)
+
+
+@pytest.mark.parametrize("T", [200, 1100])
+def test_partitioned_nvfp4_row_scales_at_an_odd_address(T):
+    """Row-major receive scales may start at any byte: a buffer at an odd address (no 16-byte
+    bulk stores possible) gets the same bytes, stored by the threads."""
+    m = moe()
+    H, E, K, P, S = 1024, 64, 8, 8, T + 8
+    w = make_case(T, H, E, K, seed=T + 7, quant="nvfp4b16", invalid_rate=0.05)
+    x, ids, wt = to_dev(w)
+    rx = filled((P, S, H // 2), torch.uint8)
+    n = P * S * (H // 16)
+    base = filled((n + 16,), torch.uint8)
+    rsf = base[1:1 + n]
+    rids = filled((P, S, K), torch.int32)
+    rw = filled((P, S, K), torch.float32)
+    st = m.new_status()
+    m.moe_dispatch_partitioned_ex("nvfp4b16", "row", x, ids, wt, E, P, rx, rsf, rids, rw, st,
+                                  input_global_scale=w.global_scale)
+    ox, osf, oids, ow = oracle.dispatch_partitioned("nvfp4b16", w.x, w.topk_ids, w.topk_weights, E, P,
+                                                    global_scale=w.global_scale, num_slots=S, fill=SENTINEL)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
+    got = base.cpu().numpy()
+    assert np.array_equal(got[1:1 + n], np.asarray(osf).reshape(-1))
+    assert got[0] == SENTINEL and np.all(got[1 + n:] == SENTINEL)
+    assert np.array_equal(rids.cpu().numpy(), oids)
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
