@@ -38,6 +38,15 @@ def test_bench_line_has_the_contract_keys():
     assert set(d["graph_replay"]) >= {"cold_l2", "warm_l2"}
 
 
+def test_graph_mode_line():
+    """--graph: the timed steps are replays of one captured step; the line says so and keeps the
+    contract keys."""
+    d = _run("--workload", "tiny", "--per-config", "none", "--steps", "4", "--warmup", "3", "--no-cpu-baseline",
+             "--no-e2e", "--graph")
+    assert d["timing"].startswith("CUDA graph of one step")
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["roofline"]["frac"] > 0
+
+
 def test_per_config_entries():
     """--per-config: each listed workload gets an entry measured in the same run, with its own
     config (the one the reference arm prints for it), step time, roofline and e2e."""
