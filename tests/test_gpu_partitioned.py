@@ -245,3 +245,52 @@ def test_partitioned_nvfp4_row_scales_at_an_odd_address(T):
     assert got[0] == SENTINEL and np.all(got[1 + n:] == SENTINEL)
     assert np.array_equal(rids.cpu().numpy(), oids)
     assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
+
+
+def test_partition_kernels_on_concurrent_streams():
+    """The ring dispatch (row-major scales), the whole-tile dispatch (swizzled scales) and the
+    ring combine of three different batches on three streams, their launches interleaved: none
+    of them keeps state outside its caller's buffers, so each stream's results match the oracle."""
+    m = moe()
+    H, E, P = 1024, 64, 8
+    specs = [(1500, 8, "row"), (1280, 6, "swizzled"), (2000, 8, "row")]
+    runs = []
+    for n, (T, K, layout) in enumerate(specs):
+        w = make_case(T, H, E, K, seed=300 + n, quant="nvfp4b16", invalid_rate=0.03)
+        x, ids, wt = to_dev(w)
+        S = T
+        rx = filled((P, S, H // 2), torch.uint8)
+        rsf = filled((m.swizzled_scale_bytes(P * S, H),) if layout == "swizzled" else (P, S, H // 16), torch.uint8)
+        rids = filled((P, S, K), torch.int32)
+        rw = filled((P, S, K), torch.float32)
+        partial_h = random_bf16(np.random.default_rng(400 + n), (P, S, H))
+        partial = torch.from_numpy(partial_h.view(np.int16)).cuda().view(torch.bfloat16)
+        out = filled((T, H), torch.bfloat16)
+        runs.append((w, layout, torch.cuda.Stream(), x, ids, wt, rx, rsf, rids, rw, partial, partial_h, out,
+                     m.new_status()))
+    torch.cuda.synchronize()
+    for step in range(2):
+        for w, layout, s, x, ids, wt, rx, rsf, rids, rw, partial, _, out, st in runs:
+            with torch.cuda.stream(s):
+                if step == 0:
+                    m.moe_dispatch_partitioned_ex("nvfp4b16", layout, x, ids, wt, E, P, rx, rsf, rids, rw, st,
+                                                  input_global_scale=w.global_scale)
+                else:
+                    m.moe_combine_partitioned(partial, ids, E, P, out, st)
+    torch.cuda.synchronize()
+    for w, layout, s, x, ids, wt, rx, rsf, rids, rw, partial, partial_h, out, st in runs:
+        assert int(st.item()) == 0
+        S = w.T
+        ox, osf, oids, ow = oracle.dispatch_partitioned("nvfp4b16", w.x, w.topk_ids, w.topk_weights, E, P,
+                                                        global_scale=w.global_scale, num_slots=S, fill=SENTINEL)
+        assert np.array_equal(bytes_of(rx), np.ascontiguousarray(ox).view(np.uint8).reshape(P, -1))
+        if layout == "swizzled":
+            want = swizzled_scales_expected(osf.reshape(P * S, H // 16), partitioned_routed(w.topk_ids, E, P, S),
+                                            partitioned_touched_rows(P, S, w.T))
+            assert np.array_equal(rsf.cpu().numpy(), want)
+        else:
+            assert np.array_equal(bytes_of(rsf), osf.reshape(P, -1))
+        assert np.array_equal(rids.cpu().numpy(), oids)
+        assert np.array_equal(rw.cpu().numpy().view(np.uint32), ow.view(np.uint32))
+        want = oracle.combine_partitioned(partial_h, w.topk_ids, E, P)
+        check_combine(bytes_of(out).view(np.uint16).reshape(w.T, H), want)
